@@ -1,0 +1,564 @@
+"""Benchmark of the batch sampler on GB300.
+
+One step = one pass of the sampling hot path over one batch: read a [B, V]
+logits matrix once, Gumbel-max sample every row, write B indices. The headline
+workload is the throughput-bound batch: bf16 logits, V = 151936, B = 256,
+N(0, 4^2) plus +6 on 32 Zipf(1.1)-ranked token ids per row, T = 1.0, per-row
+seeds from splitmix64(7), offset = decode step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. Timing: K steps replayed from CUDA graphs between CUDA
+events on the launching stream, barrier + synchronize on both sides, max over
+ranks; every step reads a different logits buffer from a pool of more than
+4x the L2 size, so no step finds its input in L2. With --gpus N > 1 (under
+torchrun) every rank samples its own batch on its own GPU: rows are independent,
+so the job is N replicas with no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "sampled rows/sec and µs/step vs V×B; achieved HBM GB/s vs 8 TB/s"
+FALLBACK_HBM_GBS = 6800.0
+HEADLINE_B = 256
+PER_ROW_PARAM_BYTES = 4 + 8 + 8 + 8  # temperature, seed, offset in; index out
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=HEADLINE_B, help="rows of the headline batch")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self, gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+        self.gpus = gpus
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(values_per_rank, times_per_rank):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return sum(values_per_rank) / max(times_per_rank)
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons around the timed
+    region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "gsample_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "token_sampling_logits_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(profile_name: str, workload_rows: int):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, scaled
+    to the benchmark's batch; None when the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_rows = re.search(r"captured_rows:\s*(\d+)", text)
+    if not (m_hash and m_bytes and m_rows) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1)) * workload_rows / int(m_rows.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def _oracle_row(args):
+    import oracle
+
+    row, dtype, T, seed, rid, off = args
+    return oracle.sample_row(row, T, seed, rid, off, dtype=dtype)[0]
+
+
+def make_pool():
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+
+    cores = os.cpu_count() or 1
+    return ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")), cores
+
+
+def oracle_rows_per_sec(pool, batch: W.Batch, rows, step: int) -> float:
+    jobs = [(np.ascontiguousarray(batch.logits[r]), batch.dtype, float(batch.temperature[r]),
+             int(batch.seed[r]), int(r), step) for r in rows]
+    t0 = time.perf_counter()
+    list(pool.map(_oracle_row, jobs, chunksize=1))
+    return len(rows) / (time.perf_counter() - t0)
+
+
+# ---------------------------------------------------------------------------
+# GPU timing
+# ---------------------------------------------------------------------------
+def _to_device(x, dtype):
+    import torch
+
+    if dtype == W.F32:
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+    return t.view(torch.bfloat16 if dtype == W.BF16 else torch.float16)
+
+
+class Runner:
+    """Timed decode steps of one workload through the C ABI, replayed from
+    captured CUDA graphs (see the module docstring for the buffer pool)."""
+
+    def __init__(self, batch: W.Batch, hlg=None, min_pool_bytes: int = 0, ring: int = 1000):
+        import ctypes
+
+        import torch
+
+        import token_sampling_logits_gb300 as gs
+
+        self.torch, self.gs, self.ctypes = torch, gs, ctypes
+        self.batch, self.hlg = batch, hlg
+        self.B, self.V = batch.B, batch.V
+        x0 = _to_device(batch.logits, batch.dtype)
+        self.bytes_per_step = x0.numel() * x0.element_size()
+        # P copies of the batch in one arena, P * bytes > min_pool_bytes, and a
+        # graph long enough to visit every copy before coming back to one.
+        self.P = max(1, math.ceil(min_pool_bytes / self.bytes_per_step) + 1) if min_pool_bytes else 1
+        arena = x0.reshape(-1).repeat(self.P)
+        n = x0.numel()
+        self.pool = [arena[k * n:(k + 1) * n].view(self.B, self.V) for k in range(self.P)]
+        self.ring = max(ring, self.P)
+        self.ring = ((self.ring + self.P - 1) // self.P) * self.P
+        self.T = torch.from_numpy(batch.temperature.astype(np.float32)).cuda()
+        self.S = gs.seeds_as_tensor(batch.seed, "cuda")
+        self.offs = torch.zeros((self.ring, self.B), dtype=torch.int64, device="cuda")
+        self.out = torch.zeros((self.ring, self.B), dtype=torch.int64, device="cuda")
+        self.ws = gs.new_workspace(self.B)
+        self.dt, _, _, self.ld = gs._logits_args(self.pool[0])
+        self.hp = hlg.to_c() if hlg is not None else None
+        self.graphs = {}
+        self.launches = 0
+
+    def _launch_range(self, n: int, k0: int):
+        L = self.gs.lib()
+        st = self.torch.cuda.current_stream().cuda_stream
+        B = self.B
+        for k in range(n):
+            x = self.pool[(k0 + k) % self.P]
+            if self.hp is None:
+                rc = L.gsample_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                             self.T.data_ptr(), self.S.data_ptr(),
+                                             self.offs.data_ptr() + 8 * B * k,
+                                             self.out.data_ptr() + 8 * B * k, self.ws.data_ptr(), st)
+            else:
+                rc = L.gsample_hlg_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                                 self.T.data_ptr(), self.S.data_ptr(),
+                                                 self.offs.data_ptr() + 8 * B * k,
+                                                 self.ctypes.byref(self.hp),
+                                                 self.out.data_ptr() + 8 * B * k,
+                                                 self.ws.data_ptr(), st)
+            if rc != 0:
+                raise RuntimeError("sampler launch failed: " + self.gs.status_string(rc))
+        self.offs.add_(n)
+
+    def graph(self, n: int):
+        torch = self.torch
+        if n not in self.graphs:
+            # buffers cycle with the step index, so a graph of n launches must
+            # start on a step that is a multiple of P to keep the cycle aligned
+            self.offs.copy_(torch.arange(self.ring, device="cuda", dtype=torch.int64)[:, None]
+                            .expand(self.ring, self.B))
+            self._launch_range(n, 0)  # warm-up, outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._launch_range(n, 0)
+            self.graphs[n] = g
+        return self.graphs[n]
+
+    def run(self, steps: int):
+        """Enqueue exactly `steps` sampler launches."""
+        full, rem = divmod(steps, self.ring)
+        if full:
+            g = self.graph(self.ring)
+            for _ in range(full):
+                g.replay()
+        if rem:
+            self.graph(rem).replay()
+        self.launches += steps
+
+    def prepare(self, steps: int):
+        full, rem = divmod(steps, self.ring)
+        if full:
+            self.graph(self.ring)
+        if rem:
+            self.graph(rem)
+        self.offs.copy_(self.torch.arange(self.ring, device="cuda", dtype=self.torch.int64)[:, None]
+                        .expand(self.ring, self.B))
+
+
+def time_steps(runner: Runner, steps: int, warmup: int, dist: Dist, clocks: ClockSampler = None):
+    torch = runner.torch
+    runner.prepare(steps)
+    runner.prepare(warmup) if warmup else None
+    if warmup:
+        runner.run(warmup)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        # keep the GPU busy while the sampler comes up, so the samples see load
+        t_end = time.perf_counter() + 0.3
+        while time.perf_counter() < t_end:
+            runner.run(min(steps, runner.ring))
+            torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    runner.run(steps)
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop() if clocks is not None else None
+    return ms, clk
+
+
+def e2e_steps(batch: W.Batch, steps: int, dist: Dist):
+    """Same metric through the public API with host buffers: every step copies
+    its logits and per-row parameters from pinned host memory, samples, and
+    copies the indices back."""
+    import torch
+
+    import token_sampling_logits_gb300 as gs
+
+    B = batch.B
+    if batch.dtype == W.F32:
+        h_x = torch.from_numpy(np.ascontiguousarray(batch.logits)).pin_memory()
+    else:
+        h_x = torch.from_numpy(np.ascontiguousarray(batch.logits).view(np.int16)).pin_memory()
+    h_T = torch.from_numpy(batch.temperature.astype(np.float32)).pin_memory()
+    h_S = torch.from_numpy(batch.seed.view(np.int64).copy()).pin_memory()
+    h_O = torch.zeros(B, dtype=torch.int64).pin_memory()
+    h_out = torch.zeros(B, dtype=torch.int64).pin_memory()
+    d_x = torch.empty(h_x.shape, dtype=h_x.dtype, device="cuda")
+    d_T = torch.empty(B, dtype=torch.float32, device="cuda")
+    d_S = torch.empty(B, dtype=torch.int64, device="cuda")
+    d_O = torch.empty(B, dtype=torch.int64, device="cuda")
+    d_out = torch.empty(B, dtype=torch.int64, device="cuda")
+    ws = gs.new_workspace(B)
+    view = (lambda t: t) if batch.dtype == W.F32 else (
+        lambda t: t.view(torch.bfloat16 if batch.dtype == W.BF16 else torch.float16))
+    h2d = h_x.numel() * h_x.element_size() + B * (4 + 8 + 8)
+    d2h = B * 8
+
+    def step(k):
+        h_O.fill_(k)
+        d_x.copy_(h_x, non_blocking=True)
+        d_T.copy_(h_T, non_blocking=True)
+        d_S.copy_(h_S, non_blocking=True)
+        d_O.copy_(h_O, non_blocking=True)
+        gs.gumbel_argmax(view(d_x), d_T, d_S, d_O, out=d_out, workspace=ws)
+        h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()  # the caller reads the tokens
+
+    for k in range(3):
+        step(k)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(steps):
+        step(k)
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    dist.barrier()
+    return secs, h2d, d2h
+
+
+def extra_table(dist: Dist, l2: int):
+    """µs/step of the other workloads (graph-replayed, rotating pools)."""
+    import token_sampling_logits_gb300 as gs
+
+    rows = []
+    cases = [("sweep", W.sweep(V, B), None) for V in W.VOCAB_SWEEP for B in W.BATCH_SWEEP]
+    cases += [("throughput", W.throughput(B), None) for B in W.THROUGHPUT_B]
+    p = W.HLG_PARAMS
+    hp = gs.HlgParams(m=p["m"], w=p["w"], beta_t=p["beta_t"], beta_h=p["beta_h"],
+                      pivot_offset=p["c"])
+    cases.append(("hlg", W.hlg(), hp))
+    cases.append(("mixed_greedy", W.mixed_greedy(), None))
+    for kind, b, h in cases:
+        r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500)
+        steps = r.ring * max(1, (2000 if b.B * b.V < 50_000_000 else 500) // r.ring)
+        ms, _ = time_steps(r, steps, 50, dist)
+        us = ms * 1000 / steps
+        nbytes = b.B * (b.V * (4 if b.dtype == W.F32 else 2) + PER_ROW_PARAM_BYTES)
+        rows.append({"workload": kind, "B": b.B, "V": b.V, "dtype": W.DTYPE_NAMES[b.dtype],
+                     "us_per_step": round(us, 3), "rows_per_s": round(b.B / us * 1e6, 1),
+                     "GBps": round(nbytes / us / 1e3, 1),
+                     "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4)})
+        del r
+    return rows
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    torch.cuda.set_device(dist.local_rank)
+    import token_sampling_logits_gb300 as gs
+
+    gs.lib()
+    # CPU baseline pool first (spawned), before the GPU is busy
+    pool = cores = None
+    batch = W.throughput(args.batch)
+    cpu = None
+    if dist.rank == 0:
+        pool, cores = make_pool()
+        sample_rows = list(range(batch.B))
+        rps = []
+        for step in range(4):
+            rps.append(oracle_rows_per_sec(pool, batch, sample_rows, step))
+        cpu = {"value": round(statistics.median(rps), 2), "unit": "rows/s", "cores": cores,
+               "kind": "oracle",
+               "sample": "%d rows x 4 decode steps of the headline batch (bf16, V=%d), one row "
+                         "per task over a spawn pool" % (batch.B, batch.V)}
+        pool.shutdown()
+
+    props = torch.cuda.get_device_properties(dist.local_rank)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    runner = Runner(batch, min_pool_bytes=4 * l2)
+    clocks = ClockSampler(dist.local_rank)
+    ms, clk = time_steps(runner, args.steps, max(3, args.warmup), dist, clocks)
+    ms = dist.max(ms)
+    secs = ms / 1000.0
+    rows_total = batch.B * args.steps * dist.world
+    value = rows_total / secs
+    us_step = ms * 1000.0 / args.steps
+    alg_bytes = batch.B * (batch.V * 2 + PER_ROW_PARAM_BYTES)
+    achieved = alg_bytes / (us_step * 1e-6) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    e2e_secs, h2d, d2h = e2e_steps(batch, args.e2e_steps, dist)
+    e2e_secs = dist.max(e2e_secs)
+    e2e_value = batch.B * args.e2e_steps * dist.world / e2e_secs
+
+    extra = None if args.no_extra or dist.rank != 0 else extra_table(Dist(1), l2)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "rows/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms / args.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "throughput bf16 V=%d B=%d (N(0,4^2) + 32 Zipf(1.1) bumps of +6, "
+                               "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
+                   "global_batch": batch.B * dist.world, "vocab": batch.V,
+                   "parallelism": "replicas x%d" % dist.world,
+                   "l2": "rotating pool of %d logits buffers (%.0f MB > 4 x L2 %.0f MB)" % (
+                       runner.P, runner.P * runner.bytes_per_step / 1e6, l2 / 1e6),
+                   "timing": "CUDA events around graph replays of %d launches" % runner.ring},
+        "us_per_step": round(us_step, 3),
+        "GBps": round(achieved, 1),
+        "frac_of_8TBps": round(achieved / 8000.0, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind + " (copy bandwidth)",
+                     "traffic": ncu_traffic("sample_kernel_bf16_throughput.md", batch.B),
+                     "kernel": "gsample::sample_kernel<bf16, 128-bit>",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if extra is not None:
+        line["workloads"] = extra
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, dist: Dist):
+    """The reference arm: the CPU oracle as it stands, on the host cores, on the
+    same workload and metric (each step a bounded sample of rows)."""
+    if dist.rank != 0:
+        return
+    batch = W.throughput(args.batch)
+    pool, cores = make_pool()
+    # calibrate, then size the per-step sample so the whole run stays in minutes
+    rps = oracle_rows_per_sec(pool, batch, list(range(min(batch.B, 2 * cores))), 0)
+    total_steps = args.steps + max(3, args.warmup)
+    budget_s = 150.0
+    rows_per_step = int(max(1, min(batch.B, budget_s * rps / total_steps)))
+    rows = list(range(rows_per_step))
+    for k in range(max(3, args.warmup)):
+        oracle_rows_per_sec(pool, batch, rows[:max(1, min(len(rows), cores))], k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        oracle_rows_per_sec(pool, batch, rows, k)
+    secs = time.perf_counter() - t0
+    pool.shutdown()
+    value = rows_per_step * args.steps / secs
+    sample = "%d of %d rows per decode step of the headline batch (bf16, V=%d), one row per " \
+             "task over a spawn pool" % (rows_per_step, batch.B, batch.V)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(secs * 1000 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "throughput bf16 V=%d B=%d (N(0,4^2) + 32 Zipf(1.1) bumps of +6, "
+                               "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
+                   "global_batch": batch.B, "vocab": batch.V, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,138 @@
+/*
+ * gsample -- batch Gumbel-max token sampling on GB300 (sm_103a).
+ *
+ * One launch samples one token per row of a [B, V] logits matrix. For every
+ * element it forms
+ *
+ *     score_i = logits[i] / T + g_i,     g_i = -log(-log u_i),
+ *
+ * and returns the index of the largest score of each row. That index is an
+ * exact sample of softmax(logits / T), with no softmax and no sort
+ * ("Softmax-free GPU sampling: Gumbel-max categorical sampling kernel",
+ * lablup/mlxcel issue #900, sections Background and Task 1). The uniform u_i
+ * comes from a stateless Philox4x32-10 stream (Salmon et al., "Parallel Random
+ * Numbers: As Easy as 1, 2, 3", SC'11) keyed by the row's 64-bit seed, with
+ * counter (i >> 2, row, offset_lo32, offset_hi32); element i takes output word
+ * i & 3; u_i = ((word >> 9) + 0.5) * 2^-23. Equal scores go to the lowest index.
+ *
+ * Conventions shared by every entry point:
+ *   - logits: device pointer to B rows of V elements (dtype below); row b starts
+ *     at element b * ld (ld >= V). Any element alignment is accepted; rows that
+ *     start on a 16-byte boundary use 128-bit loads.
+ *   - out_idx: device int64[B], written with the sampled index of each row, or
+ *     -1 for a row with no candidate (every logit -inf or NaN).
+ *   - NaN logits are never drawn; a +inf logit scores +inf (so the lowest +inf
+ *     index of a row wins); scores are formed in binary32.
+ *   - temperature / seed / offset: device arrays of B entries. A row whose
+ *     temperature is <= 0 or NaN is sampled greedily (plain argmax of the raw
+ *     logits, lowest index on ties), as the issue's Task 3 keeps greedy on argmax.
+ *   - workspace: device buffer of gsample_workspace_bytes(B) bytes, zeroed once
+ *     (gsample_workspace_init or a memset) before first use. Every launch that
+ *     completes leaves it zeroed again, so it needs no clearing between calls.
+ *     Two launches that are in flight at the same time (different streams) must
+ *     not share a workspace.
+ *   - stream: a cudaStream_t (NULL = legacy default stream). Calls only enqueue
+ *     work on it and never synchronise; GSAMPLE_OK means "launched".
+ *   - The caller owns every buffer; the library allocates nothing and keeps no
+ *     global state apart from cached device attributes.
+ *   - Errors: arguments are checked on the host before anything is launched and
+ *     a bad argument returns GSAMPLE_ERR_INVALID_ARG with nothing enqueued.
+ *     Device data (temperatures, logits) is never validated. A launch failure
+ *     returns GSAMPLE_ERR_CUDA. GSAMPLE_ERR_UNSUPPORTED means the current device
+ *     is not a compute-capability 10.3 GPU.
+ */
+#ifndef GSAMPLE_H_
+#define GSAMPLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* gsample_stream_t;
+
+typedef enum {
+  GSAMPLE_F32 = 0,  /* IEEE binary32 */
+  GSAMPLE_BF16 = 1, /* bfloat16, widened to binary32 exactly */
+  GSAMPLE_F16 = 2   /* IEEE binary16, widened to binary32 exactly */
+} gsample_dtype;
+
+typedef enum {
+  GSAMPLE_OK = 0,
+  GSAMPLE_ERR_INVALID_ARG = 1,
+  GSAMPLE_ERR_UNSUPPORTED = 2,
+  GSAMPLE_ERR_WORKSPACE = 3,
+  GSAMPLE_ERR_CUDA = 4
+} gsample_status;
+
+/* HLG pivot modes ("HLG sampling -- a piecewise tone curve on the logits",
+ * section "The pivot"). */
+typedef enum {
+  GSAMPLE_PIVOT_TOP = 0,    /* mu = l_max - pivot_offset */
+  GSAMPLE_PIVOT_ENTROPY = 1 /* mu = sum_i p_i l_i (minus the entropy) */
+} gsample_pivot_mode;
+
+/* HLG tone-curve parameters, in nats ("HLG sampling", sections "The transfer
+ * function" and "Knobs"). With z = l - mu (l = log-softmax of the row):
+ *   z < -w  : -m*w - m*beta_t*ln(1 + (-z - w)/beta_t)   (toe)
+ *   |z| <= w:  m*z                                      (linear mid)
+ *   z > w   :  m*w + m*beta_h*ln(1 + (z - w)/beta_h)    (shoulder)
+ * Requirements: m > 0 finite; w >= 0 (w = +inf turns the rolloff off);
+ * beta_t, beta_h > 0 finite; pivot_offset finite (used by the top mode). */
+typedef struct {
+  float m;
+  float w;
+  float beta_t;
+  float beta_h;
+  float pivot_offset;
+  int32_t pivot_mode; /* gsample_pivot_mode */
+} gsample_hlg_params;
+
+/* Bytes of workspace needed for B rows (16 bytes per row). */
+size_t gsample_workspace_bytes(int64_t B);
+
+/* Zero the first gsample_workspace_bytes(B) bytes of `workspace` on `stream`. */
+gsample_status gsample_workspace_init(void* workspace, int64_t B, gsample_stream_t stream);
+
+/* Greedy decoding: out_idx[b] = lowest index of the largest logit of row b
+ * (NaN and -inf never chosen; -1 if none). The issue keeps temperature 0 on a
+ * plain argmax ("Softmax-free GPU sampling", Background and Task 3); the HLG
+ * page's section "Greedy is untouched" says the same of the tone curve. */
+gsample_status gsample_argmax(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                              int64_t ld, int64_t* out_idx, void* workspace,
+                              gsample_stream_t stream);
+
+/* Gumbel-max sampling of every row in one launch ("Softmax-free GPU sampling",
+ * Task 1: per-row RNG (seed, offset), temperature, batch-wide grid).
+ * temperature[b] <= 0 or NaN selects greedy argmax for row b. */
+gsample_status gsample_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                     int64_t V, int64_t ld, const float* temperature,
+                                     const uint64_t* seed, const uint64_t* offset,
+                                     int64_t* out_idx, void* workspace,
+                                     gsample_stream_t stream);
+
+/* HLG tone curve on the row's log-probs, then Gumbel-max ("HLG sampling",
+ * sections "The transfer function", "The pivot", "Temperature semantics"):
+ *     score_i = g(l_i - mu) / T + g_i,
+ * where l = log_softmax(logits) and mu is the pivot of `hlg->pivot_mode`.
+ * Dividing the curve by T is the pages' folding of temperature into the gain.
+ * Rows with temperature <= 0 or NaN are greedy on the raw logits (the curve is
+ * monotone, so it cannot move the argmax). `hlg` is a host pointer read during
+ * the call. */
+gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                         int64_t V, int64_t ld, const float* temperature,
+                                         const uint64_t* seed, const uint64_t* offset,
+                                         const gsample_hlg_params* hlg, int64_t* out_idx,
+                                         void* workspace, gsample_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* gsample_status_string(gsample_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSAMPLE_H_ */

@@ -1,0 +1,49 @@
+/*
+ * gsample diagnostic entry points. They expose the building blocks the
+ * sampling kernels use, so that tests can compare them one by one with an
+ * independent implementation, and let a caller fix the launch shape.
+ * Same conventions as gsample.h (device pointers, caller stream, no sync).
+ */
+#ifndef GSAMPLE_DEBUG_H_
+#define GSAMPLE_DEBUG_H_
+
+#include "gsample.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw Philox4x32-10 blocks of one row's stream (Salmon et al., SC'11):
+ * out[4*j + w] = word w of the block with counter
+ * (group0 + j, row, lo32(offset), hi32(offset)) under key (lo32(seed), hi32(seed)),
+ * for j in [0, n_groups). out: device uint32[4 * n_groups]. */
+gsample_status gsample_debug_philox(uint64_t seed, uint32_t row, uint64_t offset,
+                                    int64_t group0, int64_t n_groups, uint32_t* out,
+                                    gsample_stream_t stream);
+
+/* The kernels' binary32 Gumbel transform of raw words, and the upper bound on it
+ * that the exact pruning uses: gumbel[j] = g(words[j]), bound[j] >= g(words[j])
+ * in exact arithmetic. words, gumbel, bound: device arrays of n entries; bound
+ * may be NULL. */
+gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gumbel,
+                                    float* bound, gsample_stream_t stream);
+
+/* gsample_gumbel_argmax / gsample_hlg_gumbel_argmax with an explicit number
+ * of CTAs (0 = the library's choice). ctas is clamped to [1, number of 16-byte
+ * units in the batch]. hlg == NULL selects the plain sampler. */
+gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                       int64_t V, int64_t ld, const float* temperature,
+                                       const uint64_t* seed, const uint64_t* offset,
+                                       const gsample_hlg_params* hlg, int64_t* out_idx,
+                                       void* workspace, int32_t ctas,
+                                       gsample_stream_t stream);
+
+/* Number of CTAs the library would launch for this problem (0 on bad args). */
+int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
+                                   const void* logits, int32_t hlg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSAMPLE_DEBUG_H_ */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function declared in include/*.h, and rejects
+bad arguments with the documented status before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import token_sampling_logits_gb300 as gs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"\b(gsample_[a-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function():
+    L = gs.lib()
+    names = _declared_functions()
+    assert {"gsample_argmax", "gsample_gumbel_argmax", "gsample_hlg_gumbel_argmax",
+            "gsample_workspace_bytes", "gsample_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_library_is_built_for_sm103a():
+    # cuobjdump is not used: the build flags name the one target
+    from token_sampling_logits_gb300 import build
+
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert os.path.exists(gs.library_path())
+
+
+def test_workspace_size_and_status_strings():
+    assert gs.workspace_bytes(0) == 0
+    assert gs.workspace_bytes(1) == 16
+    assert gs.workspace_bytes(512) == 16 * 512
+    seen = {gs.status_string(s) for s in range(5)}
+    assert len(seen) == 5 and all(s.startswith("GSAMPLE_") for s in seen)
+    assert "UNKNOWN" in gs.status_string(99)
+
+
+FAKE = 1 << 20  # 16-byte aligned fake device address; never dereferenced below
+
+
+def _gumbel(**kw):
+    a = dict(logits=FAKE, dtype=gs.F32, B=4, V=100, ld=100, T=FAKE, seed=FAKE, off=FAKE,
+             out=FAKE, ws=FAKE)
+    a.update(kw)
+    return gs.lib().gsample_gumbel_argmax(a["logits"], a["dtype"], a["B"], a["V"], a["ld"], a["T"],
+                                          a["seed"], a["off"], a["out"], a["ws"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(logits=None), gs.ERR_INVALID_ARG),
+    (dict(out=None), gs.ERR_INVALID_ARG),
+    (dict(ws=None), gs.ERR_INVALID_ARG),
+    (dict(T=None), gs.ERR_INVALID_ARG),
+    (dict(seed=None), gs.ERR_INVALID_ARG),
+    (dict(off=None), gs.ERR_INVALID_ARG),
+    (dict(dtype=7), gs.ERR_INVALID_ARG),
+    (dict(B=-1), gs.ERR_INVALID_ARG),
+    (dict(V=0), gs.ERR_INVALID_ARG),
+    (dict(V=1 << 31), gs.ERR_INVALID_ARG),
+    (dict(ld=99), gs.ERR_INVALID_ARG),
+    (dict(B=1 << 31), gs.ERR_INVALID_ARG),
+    (dict(logits=FAKE + 2), gs.ERR_INVALID_ARG),  # f32 logits must be 4-byte aligned
+    (dict(out=FAKE + 4), gs.ERR_INVALID_ARG),
+    (dict(ws=FAKE + 8), gs.ERR_WORKSPACE),
+    (dict(B=0), gs.OK),  # empty batch: nothing to do, nothing launched
+    (dict(B=0, logits=None, out=None, ws=None, T=None), gs.OK),
+])
+def test_invalid_arguments_rejected_on_host(kw, status):
+    assert _gumbel(**kw) == status
+
+
+def test_hlg_parameter_validation():
+    L = gs.lib()
+
+    def call(**kw):
+        p = gs.HlgParams(**{**dict(m=1.3, w=2.0, beta_t=1.0, beta_h=1.5, pivot_offset=6.0), **kw})
+        c = p.to_c()
+        return L.gsample_hlg_gumbel_argmax(FAKE, gs.F32, 0, 100, 100, FAKE, FAKE, FAKE,
+                                           ctypes.byref(c), FAKE, FAKE, None)
+
+    assert call() == gs.OK  # B = 0 after a full parameter check
+    for bad in (dict(m=0.0), dict(m=-1.0), dict(m=float("inf")), dict(w=-0.5),
+                dict(w=float("nan")), dict(beta_t=0.0), dict(beta_h=float("inf")),
+                dict(pivot_offset=float("nan")), dict(pivot_mode=5)):
+        assert call(**bad) == gs.ERR_INVALID_ARG, bad
+    assert call(w=float("inf")) == gs.OK  # rolloff off is allowed
+    assert L.gsample_hlg_gumbel_argmax(FAKE, gs.F32, 0, 100, 100, FAKE, FAKE, FAKE, None, FAKE,
+                                       FAKE, None) == gs.ERR_INVALID_ARG
+
+
+def test_no_device_is_an_error_not_a_fallback():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid-looking arguments reach the device query, which must fail loudly
+    assert _gumbel() == gs.ERR_CUDA
+    assert gs.lib().gsample_argmax(FAKE, gs.BF16, 2, 64, 64, FAKE, FAKE, None) == gs.ERR_CUDA

@@ -1,0 +1,117 @@
+"""HLG kernel vs the CPU oracle on the hlg workload recipe and edge cases,
+plus the pages' neutrality gate on the GPU ("HLG sampling", "The degeneracies
+are the safety anchors", "Correctness & evaluation" 1)."""
+import numpy as np
+import pytest
+
+import oracle
+import token_sampling_logits_gb300 as gs
+import workloads as W
+from tests import oracle_pool
+from tests.gpu_util import Tally, gpu_gumbel, gpu_hlg, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+P = W.HLG_PARAMS
+
+
+def params(mode=gs.PIVOT_TOP, **kw):
+    d = dict(m=P["m"], w=P["w"], beta_t=P["beta_t"], beta_h=P["beta_h"], pivot_offset=P["c"],
+             pivot_mode=mode)
+    d.update(kw)
+    return gs.HlgParams(**d)
+
+
+def _oracle(batch, hp, rows=None):
+    extra = dict(m=hp.m, w=hp.w, beta_t=hp.beta_t, beta_h=hp.beta_h, c=hp.pivot_offset,
+                 pivot_mode=hp.pivot_mode)
+    return oracle_pool.rows("hlg", batch.logits, batch.dtype, batch.temperature, batch.seed,
+                            batch.offset, extra=extra, row_ids=rows)
+
+
+@pytest.mark.parametrize("mode", [gs.PIVOT_TOP, gs.PIVOT_ENTROPY])
+def test_hlg_workload(mode):
+    base = W.hlg()
+    x = to_device(base.logits, base.dtype)
+    hp = params(mode)
+    t = Tally()
+    for step in (0, 1, 500):
+        b = base.at_step(step)
+        got = gpu_hlg(b, hp, logits_dev=x)
+        ref, gap = _oracle(b, hp)
+        t.add(got, ref, gap, where="hlg mode %d step %d" % (mode, step))
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16, W.F16])
+@pytest.mark.parametrize("B,V,cluster", [(1, 5, 0), (3, 100, 0), (4, 4099, 0), (2, 70001, 0),
+                                         (3, 30000, 1), (3, 30000, 2), (2, 50000, 16)])
+def test_hlg_shapes(dtype, B, V, cluster):
+    rng = np.random.default_rng([B, V, dtype])
+    x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+    x[rng.random((B, V)) < 0.01] = -np.inf
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[0] = 0.0  # greedy row
+    b = W.Batch("hlg_small", W.encode(x, dtype), dtype, T, W.splitmix64(5, B),
+                np.full(B, 9, np.uint64))
+    for mode in (gs.PIVOT_TOP, gs.PIVOT_ENTROPY):
+        hp = params(mode)
+        got = gpu_hlg(b, hp, cluster=cluster)
+        ref, gap = _oracle(b, hp)
+        Tally().add(got, ref, gap, greedy_mask=~(T > 0), where="hlg B=%d V=%d" % (B, V))
+
+
+def test_hlg_large_row_streams_twice():
+    """A row too long for the cluster's shared memory takes the re-reading path."""
+    B, V = 2, 1_500_000
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+    b = W.Batch("hlg_long", x, W.F32, np.ones(B, np.float32), W.splitmix64(6, B),
+                np.full(B, 2, np.uint64))
+    hp = params()
+    got = gpu_hlg(b, hp)
+    ref, gap = _oracle(b, hp)
+    Tally().add(got, ref, gap, where="hlg long")
+
+
+def test_hlg_special_rows():
+    B, V = 5, 999
+    x = np.random.default_rng(4).standard_normal((B, V)).astype(np.float32)
+    x[0, :] = -np.inf
+    x[1, 10] = np.inf
+    x[1, 900] = np.inf
+    x[2, ::3] = np.nan
+    x[3, :] = -np.inf
+    x[3, 998] = 0.5
+    b = W.Batch("hlg_special", x, W.F32, np.ones(B, np.float32), W.splitmix64(7, B),
+                np.full(B, 1, np.uint64))
+    for mode in (gs.PIVOT_TOP, gs.PIVOT_ENTROPY):
+        got = gpu_hlg(b, params(mode))
+        assert got[0] == -1 and got[1] == 10 and got[3] == 998
+        ref, gap = _oracle(b, params(mode))
+        Tally().add(got, ref, gap, where="hlg special")
+
+
+def test_hlg_neutrality_on_gpu():
+    """Rolloff off and m = 1: the HLG kernel draws what the plain kernel draws."""
+    base = W.sweep(65536, 8)
+    x = to_device(base.logits, base.dtype)
+    hp = params(w=float("inf"), m=1.0, pivot_offset=3.0)
+    same = total = 0
+    for step in range(5):
+        b = base.at_step(step)
+        h = gpu_hlg(b, hp, logits_dev=x)
+        g = gpu_gumbel(b, logits_dev=x)
+        ref, gap = oracle_pool.rows("gumbel", b.logits, b.dtype, b.temperature, b.seed, b.offset)
+        Tally().add(h, ref, gap, where="neutral hlg")
+        same += int((h == g).sum())
+        total += b.B
+    assert same >= total - 1
+
+
+def test_hlg_greedy_rows_untouched():
+    base = W.hlg(B=4, V=20000)
+    b = W.Batch(base.name, base.logits, base.dtype, np.zeros(4, np.float32), base.seed, base.offset)
+    got = gpu_hlg(b, params())
+    ref, _ = oracle.argmax(b.logits)
+    assert np.array_equal(got, ref)

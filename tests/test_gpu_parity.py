@@ -1,0 +1,183 @@
+"""CUDA path vs the CPU oracle, element by element, on the workloads' input
+recipes and on edge cases. Sampled rows must return the oracle's index except
+where the oracle's top-two scores are closer than 1e-5 (binary32 vs double);
+greedy rows must match exactly."""
+import numpy as np
+import pytest
+
+import oracle
+import token_sampling_logits_gb300 as gs
+import workloads as W
+from tests import oracle_pool
+from tests.gpu_util import Tally, gpu_gumbel, gpu_hlg, rows_to_device, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _oracle_rows(batch, rows=None, kind="gumbel", extra=None):
+    return oracle_pool.rows(kind, batch.logits, batch.dtype, batch.temperature, batch.seed,
+                            batch.offset, extra=extra, row_ids=rows)
+
+
+def _check_batch(batch, tally=None, rows=None, ctas=0, where=""):
+    gpu = gpu_gumbel(batch, ctas=ctas)
+    rows = np.arange(batch.B) if rows is None else np.asarray(rows)
+    ref, gap = _oracle_rows(batch, rows)
+    t = tally or Tally()
+    t.add(gpu[rows], ref, gap, greedy_mask=~(batch.temperature[rows] > 0), where=where)
+    return t
+
+
+def _small(B, V, dtype, sigma=3.0, inf_frac=0.01, seed=0, T=None):
+    rng = np.random.default_rng([seed, B, V, dtype])
+    x = (rng.standard_normal((B, V)) * sigma).astype(np.float32)
+    if inf_frac:
+        x[rng.random((B, V)) < inf_frac] = -np.inf
+    if T is None:
+        T = rng.uniform(0.3, 2.0, B).astype(np.float32)
+    return W.Batch("small", W.encode(x, dtype), dtype, np.asarray(T, np.float32),
+                   W.splitmix64(seed + 11, B), np.full(B, seed, np.uint64))
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16, W.F16])
+@pytest.mark.parametrize("B,V", [(1, 1), (3, 2), (2, 3), (5, 7), (4, 17), (7, 64), (3, 1000),
+                                 (9, 4099), (2, 65536 + 13)])
+def test_small_shapes(dtype, B, V):
+    t = Tally()
+    for step in range(3):
+        _check_batch(_small(B, V, dtype, seed=step), t, where="B=%d V=%d" % (B, V))
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 1000])
+def test_forced_cta_counts_and_split_ties(dtype, ctas):
+    """Rows split over many CTAs, with the row maximum copied to positions in
+    different CTA slices: greedy rows must still take the lowest index."""
+    B, V = 6, 20000
+    rng = np.random.default_rng(ctas)
+    x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+    x = W.roundtrip(x, dtype)
+    W.plant_ties(rng, x, range(B))
+    T = np.array([0, 0.7, 0, 1.3, 0, 0.4], np.float32)
+    b = W.Batch("ties", W.encode(x, dtype), dtype, T, W.splitmix64(3, B), np.full(B, 5, np.uint64))
+    _check_batch(b, ctas=ctas, where="ctas=%d" % ctas)
+
+
+def test_ld_and_misaligned_rows():
+    B, V, ld = 5, 3001, 3008
+    rng = np.random.default_rng(1)
+    base = (rng.standard_normal((B, ld + 8)) * 2).astype(np.float32)
+    for dtype in (W.F32, W.BF16, W.F16):
+        enc = W.encode(base, dtype)
+        dev = to_device(enc, dtype)
+        for shift in (0, 1, 3):
+            view = dev[:, shift:shift + V]  # ld = ld + 8, row start shifted by `shift` elements
+            host = np.ascontiguousarray(enc[:, shift:shift + V])
+            T = np.array([0.5, 1.0, 0.0, 2.0, 1.5], np.float32)
+            b = W.Batch("ld", host, dtype, T, W.splitmix64(9, B), np.full(B, 7, np.uint64))
+            Tt, S, O = rows_to_device(b)
+            got = gs.gumbel_argmax(view, Tt, S, O).cpu().numpy()
+            ref, gap = _oracle_rows(b)
+            Tally().add(got, ref, gap, greedy_mask=~(T > 0), where="shift=%d dt=%d" % (shift, dtype))
+
+
+def test_special_values():
+    B, V = 8, 777
+    x = np.random.default_rng(2).standard_normal((B, V)).astype(np.float32)
+    x[0, :] = -np.inf
+    x[1, :] = np.nan
+    x[2, :] = np.nan
+    x[2, 500] = -1.0  # the only candidate
+    x[3, 100] = np.inf
+    x[3, 50] = np.inf
+    x[4, ::2] = np.nan
+    x[5, :] = 0.0  # flat
+    x[6, :] = -np.inf
+    x[6, 776] = 3.0  # last element is the only candidate
+    x[7, 3] = 1e30  # huge finite logit dominates
+    for T in (1.0, 0.0):
+        b = W.Batch("special", x, W.F32, np.full(B, T, np.float32), W.splitmix64(1, B),
+                    np.full(B, 3, np.uint64))
+        got = gpu_gumbel(b)
+        ref, gap = _oracle_rows(b)
+        assert got[0] == -1 and got[1] == -1
+        assert got[2] == 500 and got[3] == 50 and got[6] == 776 and got[7] == 3
+        Tally().add(got, ref, gap, greedy_mask=np.full(B, T <= 0), where="T=%g" % T)
+
+
+def test_temperature_edge_values_route_to_greedy():
+    B, V = 6, 4096
+    b = _small(B, V, W.F32, seed=4, T=np.array([0.0, -1.0, np.nan, -0.0, 1e-30, 3.0], np.float32))
+    got = gpu_gumbel(b)
+    ref, _ = oracle.argmax(b.logits)
+    assert np.array_equal(got[:4], ref[:4])
+
+
+def test_argmax_entry_matches_library_argmax():
+    for dtype in (W.F32, W.BF16, W.F16):
+        b = _small(33, 12345, dtype, seed=8)
+        x = to_device(b.logits, dtype)
+        got = gs.argmax(x).cpu().numpy()
+        ref, _ = oracle.argmax(b.logits, dtype=dtype)
+        assert np.array_equal(got, ref)
+        # torch's argmax returns the first maximal index on this NaN-free data
+        xm = x.float().masked_fill(torch.isneginf(x.float()), -3e38)
+        assert np.array_equal(got, xm.argmax(dim=1).cpu().numpy())
+
+
+def test_workspace_left_clean_and_deterministic():
+    b = _small(16, 50000, W.BF16, seed=6)
+    ws = gs.new_workspace(b.B)
+    x = to_device(b.logits, b.dtype)
+    a1 = gpu_gumbel(b, logits_dev=x, workspace=ws)
+    assert int(ws.count_nonzero()) == 0
+    a2 = gpu_gumbel(b, logits_dev=x, workspace=ws)
+    assert np.array_equal(a1, a2)
+    b2 = b.at_step(1)
+    a3 = gpu_gumbel(b2, logits_dev=x, workspace=ws)
+    assert not np.array_equal(a1, a3)
+
+
+@pytest.mark.parametrize("V", W.VOCAB_SWEEP)
+@pytest.mark.parametrize("B", W.BATCH_SWEEP)
+def test_sweep_workload(V, B):
+    base = W.sweep(V, B)
+    t = Tally()
+    x = to_device(base.logits, base.dtype)
+    for step in (0, 1, 999):
+        b = base.at_step(step)
+        got = gpu_gumbel(b, logits_dev=x)
+        ref, gap = _oracle_rows(b)
+        t.add(got, ref, gap, where="sweep V=%d B=%d step %d" % (V, B, step))
+
+
+@pytest.mark.parametrize("B", W.THROUGHPUT_B)
+def test_throughput_workload_sampled_rows(B):
+    """Full-size bf16 batches in the launch configuration the benchmark times;
+    the oracle scores a sample of rows one by one."""
+    base = W.throughput(B)
+    x = to_device(base.logits, base.dtype)
+    rows = np.unique(np.r_[0, B - 1, np.random.default_rng(B).choice(B, 14, replace=False)])
+    t = Tally()
+    for step in (0, 57):
+        b = base.at_step(step)
+        got = gpu_gumbel(b, logits_dev=x)
+        ref, gap = _oracle_rows(b, rows)
+        t.add(got[rows], ref, gap, where="throughput B=%d step %d" % (B, step))
+
+
+def test_mixed_greedy_workload():
+    base = W.mixed_greedy()
+    x = to_device(base.logits, base.dtype)
+    greedy = ~(base.temperature > 0)
+    for step in (0, 42):
+        b = base.at_step(step)
+        got = gpu_gumbel(b, logits_dev=x)
+        # every greedy row, byte-exact (ties planted on rows 0, 2, 4, 6)
+        gref, _ = oracle.argmax(b.logits, dtype=b.dtype)
+        assert np.array_equal(got[greedy], gref[greedy])
+        rows = np.r_[1, 3, 5, 7, np.random.default_rng(step).choice(np.arange(9, 512, 2), 12,
+                                                                     replace=False)]
+        ref, gap = _oracle_rows(b, rows)
+        Tally().add(got[rows], ref, gap, where="mixed step %d" % step)

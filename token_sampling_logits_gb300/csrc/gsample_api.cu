@@ -1,0 +1,336 @@
+// Host side of the C ABI declared in include/gsample.h and include/gsample_debug.h:
+// argument checks, launch planning and status mapping. Nothing here touches
+// device data or synchronises; every entry point only enqueues on the caller's
+// stream.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gsample.h"
+#include "gsample_debug.h"
+#include "gsample_internal.h"
+
+namespace {
+
+using gsample::SampleParams;
+using gsample::HlgParams;
+using gsample::WsRow;
+
+// Largest V: element indices, Philox group indices and the packed key's low
+// word all stay in 32 bits with room for a 16-byte unit past the end.
+constexpr int64_t kMaxV = (int64_t(1) << 31) - 128;
+constexpr int64_t kMaxB = INT32_MAX;
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMinUnitsPerCta = gsample::kThreads;  // at least one unit per thread
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  int sample_slots[6] = {0, 0, 0, 0, 0, 0};  // CTAs per SM, per (dtype, vec)
+  int hlg_cluster[6] = {0, 0, 0, 0, 0, 0};   // largest co-schedulable cluster, per (dtype, vec)
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+gsample_status device_info(const DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GSAMPLE_ERR_CUDA;
+    }
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.supported) {
+      for (int dt = 0; dt < 3; ++dt)
+        for (int v = 0; v < 2; ++v) {
+          const int n = gsample::sample_ctas_per_sm(dt, v != 0);
+          if (n <= 0) {
+            cudaGetLastError();
+            return GSAMPLE_ERR_CUDA;
+          }
+          d.sample_slots[dt * 2 + v] = n;
+          const int c = gsample::hlg_max_cluster(dt, v != 0, gsample::hlg_smem_limit());
+          if (c <= 0) {
+            cudaGetLastError();
+            return GSAMPLE_ERR_CUDA;
+          }
+          d.hlg_cluster[dt * 2 + v] = c;
+        }
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.supported ? GSAMPLE_OK : GSAMPLE_ERR_UNSUPPORTED;
+}
+
+int64_t elt_bytes(gsample_dtype dt) { return dt == GSAMPLE_F32 ? 4 : 2; }
+
+gsample_status check_common(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                            int64_t ld, const int64_t* out_idx, const void* ws) {
+  if (dtype != GSAMPLE_F32 && dtype != GSAMPLE_BF16 && dtype != GSAMPLE_F16)
+    return GSAMPLE_ERR_INVALID_ARG;
+  if (B < 0 || B > kMaxB || V < 1 || V > kMaxV || ld < V) return GSAMPLE_ERR_INVALID_ARG;
+  if (B == 0) return GSAMPLE_OK;
+  if (!logits || !out_idx || !ws) return GSAMPLE_ERR_INVALID_ARG;
+  const int64_t e = elt_bytes(dtype);
+  if (ld > INT64_MAX / e / B) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)logits % (uintptr_t)e) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)out_idx % 8) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)ws % 16) return GSAMPLE_ERR_WORKSPACE;
+  return GSAMPLE_OK;
+}
+
+bool vec_path(const void* logits, gsample_dtype dtype, int64_t ld) {
+  return ((uintptr_t)logits % 16 == 0) && ((ld * elt_bytes(dtype)) % 16 == 0);
+}
+
+// Fill SampleParams and choose the CTA count: one wave of CTAs (SMs x resident
+// CTAs per SM), fewer when the batch has too few units to give every thread one.
+void plan_sample(const DeviceInfo& d, const void* logits, gsample_dtype dtype, int64_t B,
+                 int64_t V, int64_t ld, int32_t ctas_override, SampleParams* p, bool* vec_out) {
+  const bool vec = vec_path(logits, dtype, ld);
+  const int epu = gsample::units_elems((int)dtype, vec);
+  const int64_t nu = (V + epu - 1) / epu;
+  const int64_t total = B * nu;
+  int64_t g;
+  if (ctas_override > 0) {
+    g = ctas_override;
+  } else {
+    const int64_t slots = (int64_t)d.sms * d.sample_slots[(int)dtype * 2 + (vec ? 1 : 0)];
+    g = (total + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
+    if (g > slots) g = slots;
+  }
+  if (g > total) g = total;
+  if (g < 1) g = 1;
+  std::memset(p, 0, sizeof *p);
+  p->logits = static_cast<const char*>(logits);
+  p->ld_bytes = ld * elt_bytes(dtype);
+  p->B = B;
+  p->V = (int32_t)V;
+  p->units_per_row = (int32_t)nu;
+  p->total_units = total;
+  p->ctas = (int32_t)g;
+  *vec_out = vec;
+}
+
+gsample_status run_sample(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                          int64_t ld, const float* temperature, const uint64_t* seed,
+                          const uint64_t* offset, int64_t* out_idx, void* workspace,
+                          int32_t ctas_override, cudaStream_t stream) {
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (st != GSAMPLE_OK || B == 0) return st;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  SampleParams p;
+  bool vec = false;
+  plan_sample(*d, logits, dtype, B, V, ld, ctas_override, &p, &vec);
+  p.temperature = temperature;
+  p.seed = seed;
+  p.offset = offset;
+  p.out_idx = out_idx;
+  p.ws = static_cast<WsRow*>(workspace);
+  const cudaError_t err = gsample::launch_sample(p, (int)dtype, vec, stream);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status check_hlg(const gsample_hlg_params* h) {
+  if (!h) return GSAMPLE_ERR_INVALID_ARG;
+  const bool ok = std::isfinite(h->m) && h->m > 0.0f && h->w >= 0.0f && !std::isnan(h->w) &&
+                  std::isfinite(h->beta_t) && h->beta_t > 0.0f && std::isfinite(h->beta_h) &&
+                  h->beta_h > 0.0f && std::isfinite(h->pivot_offset) &&
+                  (h->pivot_mode == GSAMPLE_PIVOT_TOP || h->pivot_mode == GSAMPLE_PIVOT_ENTROPY);
+  return ok ? GSAMPLE_OK : GSAMPLE_ERR_INVALID_ARG;
+}
+
+gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
+                       const float* temperature, const uint64_t* seed, const uint64_t* offset,
+                       const gsample_hlg_params* hlg, int64_t* out_idx, void* workspace,
+                       int32_t ctas_override, cudaStream_t stream) {
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (st != GSAMPLE_OK) return st;
+  if (check_hlg(hlg) != GSAMPLE_OK || !temperature || !seed || !offset)
+    return GSAMPLE_ERR_INVALID_ARG;
+  if (B == 0) return GSAMPLE_OK;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+
+  const bool vec = vec_path(logits, dtype, ld);
+  const int epu = gsample::units_elems((int)dtype, vec);
+  const int64_t nu = (V + epu - 1) / epu;
+  // Smallest cluster whose CTAs can each hold their slice of the row on chip;
+  // if even the largest cluster cannot, the slices stream from memory twice.
+  int cluster = ctas_override > 0 ? ctas_override : 0;
+  if (cluster == 0) {
+    const int max_cluster = d->hlg_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
+    cluster = max_cluster < 1 ? 1 : max_cluster;
+    // Prefer spreading a row over the whole cluster when B is small (latency),
+    // but never more CTAs per row than units / threads.
+    int64_t cap = (nu + gsample::kThreads - 1) / gsample::kThreads;
+    if (cap < 1) cap = 1;
+    if (cluster > cap) cluster = (int)cap;
+  }
+  if (cluster > 16 || cluster > d->hlg_cluster[(int)dtype * 2 + (vec ? 1 : 0)])
+    return GSAMPLE_ERR_INVALID_ARG;
+  HlgParams p;
+  std::memset(&p, 0, sizeof p);
+  p.logits = static_cast<const char*>(logits);
+  p.ld_bytes = ld * elt_bytes(dtype);
+  p.B = B;
+  p.V = (int32_t)V;
+  p.units_per_row = (int32_t)nu;
+  p.cluster = cluster;
+  p.units_per_cta = (int32_t)((nu + cluster - 1) / cluster);
+  p.temperature = temperature;
+  p.seed = seed;
+  p.offset = offset;
+  p.out_idx = out_idx;
+  p.ws = static_cast<WsRow*>(workspace);
+  p.m = hlg->m;
+  p.w = hlg->w;
+  p.beta_t = hlg->beta_t;
+  p.beta_h = hlg->beta_h;
+  p.pivot_offset = hlg->pivot_offset;
+  p.pivot_mode = hlg->pivot_mode;
+  const cudaError_t err = gsample::launch_hlg(p, (int)dtype, vec, stream);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gsample_workspace_bytes(int64_t B) {
+  return B > 0 ? (size_t)B * sizeof(WsRow) : 0;
+}
+
+gsample_status gsample_workspace_init(void* workspace, int64_t B, gsample_stream_t stream) {
+  if (B < 0 || B > kMaxB) return GSAMPLE_ERR_INVALID_ARG;
+  if (B == 0) return GSAMPLE_OK;
+  if (!workspace) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)workspace % 16) return GSAMPLE_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, gsample_workspace_bytes(B), (cudaStream_t)stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status gsample_argmax(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                              int64_t ld, int64_t* out_idx, void* workspace,
+                              gsample_stream_t stream) {
+  return run_sample(logits, dtype, B, V, ld, nullptr, nullptr, nullptr, out_idx, workspace, 0,
+                    (cudaStream_t)stream);
+}
+
+gsample_status gsample_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                     int64_t V, int64_t ld, const float* temperature,
+                                     const uint64_t* seed, const uint64_t* offset,
+                                     int64_t* out_idx, void* workspace,
+                                     gsample_stream_t stream) {
+  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
+  return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
+                    (cudaStream_t)stream);
+}
+
+gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                         int64_t V, int64_t ld, const float* temperature,
+                                         const uint64_t* seed, const uint64_t* offset,
+                                         const gsample_hlg_params* hlg, int64_t* out_idx,
+                                         void* workspace, gsample_stream_t stream) {
+  return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, out_idx, workspace, 0,
+                 (cudaStream_t)stream);
+}
+
+const char* gsample_status_string(gsample_status status) {
+  switch (status) {
+    case GSAMPLE_OK: return "GSAMPLE_OK";
+    case GSAMPLE_ERR_INVALID_ARG: return "GSAMPLE_ERR_INVALID_ARG: invalid argument";
+    case GSAMPLE_ERR_UNSUPPORTED: return "GSAMPLE_ERR_UNSUPPORTED: device is not compute capability 10.3";
+    case GSAMPLE_ERR_WORKSPACE: return "GSAMPLE_ERR_WORKSPACE: workspace missing or misaligned";
+    case GSAMPLE_ERR_CUDA: return "GSAMPLE_ERR_CUDA: CUDA runtime error";
+  }
+  return "GSAMPLE_ERR_UNKNOWN";
+}
+
+gsample_status gsample_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
+                                    int64_t n_groups, uint32_t* out, gsample_stream_t stream) {
+  if (n_groups < 0 || group0 < 0 || !out || (uintptr_t)out % 16) return GSAMPLE_ERR_INVALID_ARG;
+  if (n_groups == 0) return GSAMPLE_OK;
+  const DeviceInfo* d = nullptr;
+  const gsample_status st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  if (gsample::launch_debug_philox(seed, row, offset, group0, n_groups, out,
+                                   (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gumbel, float* bound,
+                                    gsample_stream_t stream) {
+  if (n < 0 || !words || !gumbel) return GSAMPLE_ERR_INVALID_ARG;
+  if (n == 0) return GSAMPLE_OK;
+  const DeviceInfo* d = nullptr;
+  const gsample_status st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  if (gsample::launch_debug_gumbel(words, n, gumbel, bound, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                       int64_t V, int64_t ld, const float* temperature,
+                                       const uint64_t* seed, const uint64_t* offset,
+                                       const gsample_hlg_params* hlg, int64_t* out_idx,
+                                       void* workspace, int32_t ctas, gsample_stream_t stream) {
+  if (ctas < 0) return GSAMPLE_ERR_INVALID_ARG;
+  if (hlg)
+    return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, out_idx, workspace,
+                   ctas, (cudaStream_t)stream);
+  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
+  return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, ctas,
+                    (cudaStream_t)stream);
+}
+
+int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
+                                   const void* logits, int32_t hlg) {
+  if (check_common(logits ? logits : (const void*)16, dtype, B, V, ld, (const int64_t*)16,
+                   (const void*)16) != GSAMPLE_OK || B == 0 || hlg)
+    return 0;
+  const DeviceInfo* d = nullptr;
+  if (device_info(&d) != GSAMPLE_OK) return 0;
+  SampleParams p;
+  bool vec = false;
+  plan_sample(*d, logits ? logits : (const void*)16, dtype, B, V, ld, 0, &p, &vec);
+  return p.ctas;
+}
+
+}  // extern "C"

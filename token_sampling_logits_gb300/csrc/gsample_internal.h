@@ -1,0 +1,69 @@
+// Internal interface between the host API (gsample_api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "gsample_device.cuh"
+
+namespace gsample {
+
+// One launch of the row sampler. Rows are cut into 16-byte units (or 4-element
+// units when a row does not start on a 16-byte boundary); the B * units_per_row
+// units are split into `ctas` near-equal contiguous ranges, one per CTA.
+struct SampleParams {
+  const char* logits;
+  int64_t ld_bytes;
+  int64_t B;
+  int32_t V;
+  int32_t units_per_row;
+  int64_t total_units;
+  int32_t ctas;
+  const float* temperature;  // nullptr: every row greedy
+  const uint64_t* seed;
+  const uint64_t* offset;
+  int64_t* out_idx;
+  WsRow* ws;
+};
+
+// HLG launch: one thread-block cluster of `cluster` CTAs per row.
+struct HlgParams {
+  const char* logits;
+  int64_t ld_bytes;
+  int64_t B;
+  int32_t V;
+  int32_t units_per_row;
+  int32_t cluster;
+  int32_t units_per_cta;  // slice of the row held by each CTA of the cluster
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  int64_t* out_idx;
+  WsRow* ws;
+  float m, w, beta_t, beta_h, pivot_offset;
+  int32_t pivot_mode;
+};
+
+// Elements per unit for a dtype code (0 f32, 1 bf16, 2 f16) and load path.
+inline int units_elems(int dtype, bool vec) { return vec ? (dtype == 0 ? 4 : 8) : 4; }
+
+// Occupancy-derived CTA slots per SM for the sampler kernel of (dtype, vec).
+int sample_ctas_per_sm(int dtype, bool vec);
+size_t sample_smem_bytes(int dtype, bool vec);
+cudaError_t launch_sample(const SampleParams& p, int dtype, bool vec, cudaStream_t stream);
+
+// HLG: the largest cluster size the device can co-schedule for this kernel and
+// the shared memory a CTA needs to hold `units_per_cta` units.
+int hlg_max_cluster(int dtype, bool vec, size_t smem_bytes);
+size_t hlg_smem_bytes(int dtype, bool vec, int32_t units_per_cta);
+size_t hlg_smem_limit();
+cudaError_t launch_hlg(const HlgParams& p, int dtype, bool vec, cudaStream_t stream);
+
+cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
+                                int64_t n, uint32_t* out, cudaStream_t stream);
+cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, float* bound,
+                                cudaStream_t stream);
+
+}  // namespace gsample
