@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=HEADLINE_B, help="rows of the headline batch")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--quick", action="store_true",
+                    help="headline timing only (no CPU baseline, e2e, clocks or table); for "
+                         "profiler runs")
     return ap.parse_args()
 
 
@@ -435,7 +438,7 @@ def run_ours(args, dist: Dist):
     pool = cores = None
     batch = W.throughput(args.batch)
     cpu = None
-    if dist.rank == 0:
+    if dist.rank == 0 and not args.quick:
         pool, cores = make_pool()
         sample_rows = list(range(batch.B))
         rps = []
@@ -450,7 +453,7 @@ def run_ours(args, dist: Dist):
     props = torch.cuda.get_device_properties(dist.local_rank)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     runner = Runner(batch, min_pool_bytes=4 * l2)
-    clocks = ClockSampler(dist.local_rank)
+    clocks = None if args.quick else ClockSampler(dist.local_rank)
     ms, clk = time_steps(runner, args.steps, max(3, args.warmup), dist, clocks)
     ms = dist.max(ms)
     secs = ms / 1000.0
@@ -461,11 +464,14 @@ def run_ours(args, dist: Dist):
     achieved = alg_bytes / (us_step * 1e-6) / 1e9
     peak, peak_kind = hbm_peak()
 
-    e2e_secs, h2d, d2h = e2e_steps(batch, args.e2e_steps, dist)
-    e2e_secs = dist.max(e2e_secs)
-    e2e_value = batch.B * args.e2e_steps * dist.world / e2e_secs
+    e2e = None
+    if not args.quick:
+        e2e_secs, h2d, d2h = e2e_steps(batch, args.e2e_steps, dist)
+        e2e_secs = dist.max(e2e_secs)
+        e2e = {"value": round(batch.B * args.e2e_steps * dist.world / e2e_secs, 1),
+               "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    extra = None if args.no_extra or dist.rank != 0 else extra_table(Dist(1), l2)
+    extra = None if args.no_extra or args.quick or dist.rank != 0 else extra_table(Dist(1), l2)
 
     line = {
         "metric": METRIC,
@@ -497,8 +503,7 @@ def run_ours(args, dist: Dist):
                      "kernel": "gsample::sample_kernel<bf16, 128-bit>",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 1), "unit": "rows/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk,
     }
