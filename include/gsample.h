@@ -131,6 +131,36 @@ gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype
 /* Static, human-readable name of a status code. */
 const char* gsample_status_string(gsample_status status);
 
+/* Largest batch gsample_gumbel_argmax_static accepts. */
+#define GSAMPLE_STATIC_WS_MAX_ROWS 4096
+
+/* gsample_gumbel_argmax without a workspace argument: the merge state lives in
+ * a fixed array inside the library (GSAMPLE_STATIC_WS_MAX_ROWS rows, 64 KiB),
+ * so the call allocates no device memory. The source pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate: code that
+ * runs inside a host framework or engine plugin which owns all device memory
+ * and forbids allocations while it executes, code with a device-memory budget
+ * fixed at start-up, and decode loops where cudaMalloc/cudaFree would stall the
+ * GPU with their implicit synchronisation.
+ *   - The caller still passes the inputs and out_idx (same meaning as in
+ *     gsample_gumbel_argmax); B > GSAMPLE_STATIC_WS_MAX_ROWS returns
+ *     GSAMPLE_ERR_INVALID_ARG with nothing enqueued; B == 0 is a no-op.
+ *   - The array is held by every GPU that loads the library until the process
+ *     exits. The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) and zeroes it, synchronously; make that first call
+ *     before any stream capture begins. A failed set-up returns
+ *     GSAMPLE_ERR_CUDA.
+ *   - Every call clears the rows it uses (an asynchronous memset on `stream`)
+ *     before sampling, and calls no cudaMalloc, cudaFree or other allocating
+ *     routine.
+ *   - All calls on a device share the one array: calls whose work overlaps on
+ *     the GPU (different streams, or host threads racing) race on it and may
+ *     return wrong indices. Serialise them, for example on one stream. */
+gsample_status gsample_gumbel_argmax_static(const void* logits, gsample_dtype dtype, int64_t B,
+                                            int64_t V, int64_t ld, const float* temperature,
+                                            const uint64_t* seed, const uint64_t* offset,
+                                            int64_t* out_idx, gsample_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
