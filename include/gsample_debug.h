@@ -22,9 +22,9 @@ gsample_status gsample_debug_philox(uint64_t seed, uint32_t row, uint64_t offset
                                     gsample_stream_t stream);
 
 /* The kernels' binary32 Gumbel transform of raw words, and the upper bound on it
- * that the exact pruning uses: gumbel[j] = g(words[j]), bound[j] >= g(words[j])
- * in exact arithmetic. words, gumbel, bound: device arrays of n entries; bound
- * may be NULL. */
+ * that the exact pruning relies on: gumbel[j] = g(words[j]) and
+ * bound[j] = -log(1 - u(words[j])), which is >= g(words[j]) in exact arithmetic.
+ * words, gumbel, bound: device arrays of n entries; bound may be NULL. */
 gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gumbel,
                                     float* bound, gsample_stream_t stream);
 

@@ -52,5 +52,5 @@ def test_gumbel_transform_all_cells():
     assert err.max() < 2e-6, err.max()
     # the pruning constants: max g below 16.64, and the per-word bound holds
     assert g.max() < 16.64
-    assert np.all(bound >= ref - 1e-6)
+    assert np.all(bound >= ref - 4e-6)  # -log(1-u) >= g exactly; binary32 rounding aside
     assert np.all(g <= bound + 1e-3)

@@ -124,6 +124,7 @@ void plan_sample(const DeviceInfo& d, const void* logits, gsample_dtype dtype, i
   p->units_per_row = (int32_t)nu;
   p->total_units = total;
   p->ctas = (int32_t)g;
+  p->warps = g * gsample::kWarps < total ? g * gsample::kWarps : total;
   *vec_out = vec;
 }
 

@@ -51,6 +51,80 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The blocks of one row share counter words 1..3 (row, lo32(offset),
+// hi32(offset)) and the key, so in the first two rounds one of the two
+// multiplies does not depend on the group index: it is done once per row.
+//   round 0: (h0, l0) = M0 * g          ->  (u1, L1, h0 ^ u2, l0)
+//   round 1: (h1, l1) = M1 * (h0 ^ u2)  ->  (h1 ^ u3, l1, l0 ^ u4, w2)
+// with (H1, L1) = M1 * off0, u1 = H1 ^ row ^ k0, u2 = off1 ^ k1,
+// u3 = L1 ^ (k0 + W0), (H0, w2) = M0 * u1, u4 = H0 ^ (k1 + W1).
+// Rounds 2..9 then run as usual. The result equals philox4x32_10 on
+// (g, row, off0, off1).
+struct PhiloxRow {
+  uint32_t k0, k1, u2, u3, u4, w2;
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t row, uint32_t off0, uint32_t off1,
+                                                uint32_t k0, uint32_t k1) {
+  const unsigned long long p1 = (unsigned long long)kPhiloxM1 * off0;
+  const uint32_t u1 = (uint32_t)(p1 >> 32) ^ row ^ k0;
+  const unsigned long long p0 = (unsigned long long)kPhiloxM0 * u1;
+  PhiloxRow r;
+  r.k0 = k0;
+  r.k1 = k1;
+  r.u2 = off1 ^ k1;
+  r.u3 = (uint32_t)p1 ^ (k0 + kPhiloxW0);
+  r.u4 = (uint32_t)(p0 >> 32) ^ (k1 + kPhiloxW1);
+  r.w2 = (uint32_t)p0;
+  return r;
+}
+
+// Four blocks of a row (groups g[0..3]), interleaved round by round.
+__device__ __forceinline__ void philox_row_x4(const uint32_t (&g)[4], const PhiloxRow& pr,
+                                              uint4 (&out)[4]) {
+  uint4 c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const unsigned long long a = (unsigned long long)kPhiloxM0 * g[j];
+    const uint32_t z = (uint32_t)(a >> 32) ^ pr.u2;
+    const unsigned long long b = (unsigned long long)kPhiloxM1 * z;
+    c[j] = make_uint4((uint32_t)(b >> 32) ^ pr.u3, (uint32_t)b, (uint32_t)a ^ pr.u4, pr.w2);
+  }
+  uint32_t k0 = pr.k0 + 2u * kPhiloxW0, k1 = pr.k1 + 2u * kPhiloxW1;
+#pragma unroll
+  for (int round = 2; round < 10; ++round) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const unsigned long long p0 = (unsigned long long)kPhiloxM0 * c[j].x;
+      const unsigned long long p1 = (unsigned long long)kPhiloxM1 * c[j].z;
+      c[j] = make_uint4((uint32_t)(p1 >> 32) ^ c[j].y ^ k0, (uint32_t)p1,
+                        (uint32_t)(p0 >> 32) ^ c[j].w ^ k1, (uint32_t)p0);
+    }
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) out[j] = c[j];
+}
+
+__device__ __forceinline__ uint4 philox_row_1(uint32_t g, const PhiloxRow& pr) {
+  const unsigned long long a = (unsigned long long)kPhiloxM0 * g;
+  const uint32_t z = (uint32_t)(a >> 32) ^ pr.u2;
+  const unsigned long long b = (unsigned long long)kPhiloxM1 * z;
+  uint4 c = make_uint4((uint32_t)(b >> 32) ^ pr.u3, (uint32_t)b, (uint32_t)a ^ pr.u4, pr.w2);
+  uint32_t k0 = pr.k0 + 2u * kPhiloxW0, k1 = pr.k1 + 2u * kPhiloxW1;
+#pragma unroll
+  for (int round = 2; round < 10; ++round) {
+    const unsigned long long p0 = (unsigned long long)kPhiloxM0 * c.x;
+    const unsigned long long p1 = (unsigned long long)kPhiloxM1 * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                   (uint32_t)p0);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
   return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
@@ -70,14 +144,10 @@ __device__ __forceinline__ float gumbel_of_word(uint32_t r) {
   return -logf(-logf(uniform_open(r)));
 }
 
-// Upper bound on g(r) from integer/bit operations only. With v = 1 - u (also
-// exact, the same construction on ~r): -log u >= v, so g <= -ln v; and writing
-// v = 2^e (1 + f), -log2 v = -e - log2(1 + f) <= -e - f, which is
-// (bits(1.0f) - bits(v)) / 2^23. Hence g <= (bits(1) - bits(v)) * ln2 / 2^23.
+// The bound on g that the pruning relies on: -log u >= 1 - u = v, hence
+// g = -log(-log u) <= -log v (v is formed exactly, like u, from ~r).
 __device__ __forceinline__ float gumbel_bound_of_word(uint32_t r) {
-  const float v = uniform_open(~r);
-  const uint32_t d = 0x3F800000u - __float_as_uint(v);
-  return __uint2float_rn(d) * (0.69314718f / 8388608.0f);
+  return -logf(uniform_open(~r));
 }
 
 // Largest binary32 Gumbel value the kernels can produce is 16.6355 (at
@@ -131,6 +201,15 @@ __device__ __forceinline__ void warp_argmax(float& s, int32_t& i) {
   }
 }
 
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Exact pruning. Given L, the exact score of some element of the row, an element
 // whose score cannot reach L cannot be the row's argmax. For x < thr_x the
@@ -144,6 +223,32 @@ struct Prune {
   float lm;     // skip when x * (1/T) + bound(g) < lm
   bool use_bound;
 };
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Once the Philox word w of an element is known: can x/T + g(w) still reach L?
+// Because -log u >= 1 - u = v, g = -log(-log u) <= -log v, so reaching L needs
+// v <= exp(x/T - L). The pruning margins are folded into lm; the test is
+// evaluated as v <= 2^(x*a + c) with a = log2(e)/T and c = -lm*log2(e). The
+// approximate exponential errs by about 1e-7 relative, far inside the e^0.01
+// slack of lm. NaN or -inf logits never pass; +inf always does. Without a finite
+// L (use_bound false) the caller falls back to x >= thr_x.
+struct ReachTest {
+  float a, c;
+};
+
+__device__ __forceinline__ ReachTest make_reach(const Prune& p, float rT) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  return ReachTest{rT * kLog2e, -p.lm * kLog2e};
+}
+
+__device__ __forceinline__ bool may_reach(float x, uint32_t w, const ReachTest& t) {
+  return uniform_open(~w) <= ex2_approx(fmaf(x, t.a, t.c));
+}
 
 __device__ __forceinline__ Prune make_prune(float L, float T) {
   Prune p;

@@ -21,6 +21,7 @@ struct SampleParams {
   int32_t units_per_row;
   int64_t total_units;
   int32_t ctas;
+  int64_t warps;  // warps that get a non-empty range: min(ctas * kWarps, total_units)
   const float* temperature;  // nullptr: every row greedy
   const uint64_t* seed;
   const uint64_t* offset;

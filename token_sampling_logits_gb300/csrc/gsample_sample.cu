@@ -4,31 +4,51 @@
 // logits/T + g, g = -log(-log u) from a per-(row, element) counter stream,
 // one index-carrying max per row, all rows in one grid).
 //
-// Work split. The B rows are cut into 16-byte units and the B * units_per_row
-// units are dealt to exactly one wave of CTAs in near-equal contiguous ranges,
-// so the work per CTA is balanced whatever B and V are. A CTA walks the rows its
-// range touches; each of its warps takes an equal contiguous piece of the
-// row segment and streams it in tiles of 32 lanes x kVPT units (each load
-// instruction of a warp covers 512 contiguous bytes).
+// Work split. The B rows are cut into 16-byte units. All B * units_per_row
+// units are dealt to the warps of one wave of CTAs, in near-equal contiguous
+// ranges. Each warp walks its range in tiles of 32 lanes x kVPT units; a tile
+// never crosses a row. Warps never wait for one another: there is no CTA-wide
+// barrier in the kernel.
 //
-// Merge. A row's candidates meet in its workspace slot: an atomicMax on a packed
-// (ordered score, ~index) 64-bit key, then a ticket; the last CTA of the row
-// writes out_idx and clears the slot. No CTA ever waits for another.
+// Memory pipeline. Each warp streams its tiles through a ring of kStages tiles
+// in shared memory with cp.async (L2 evict-first hint; each warp instruction
+// moves 512 contiguous bytes), so kStages-1 tiles are in flight while the warp
+// computes on the current one, across row boundaries, without holding the data
+// in registers.
+//
+// Merge. When a warp finishes its part of a row it folds its best (score,
+// index) into the row's workspace slot with atomicMax on a packed 64-bit key,
+// then takes a ticket; the warp that completes the row's count writes out_idx
+// and clears the slot.
 //
 // Exact pruning (sampled rows). Each warp keeps L, the best exact score known
-// for the row (its own candidates and whatever other CTAs have published into
-// the row's key). An element with x/T + max(g) < L cannot win, so Philox and
-// the logarithms are skipped for it. Surviving 4-element groups are compacted
-// across the warp through shared memory so that all 32 lanes run Philox on
-// useful work.
+// for the row (its own candidates and whatever other warps have published). An
+// element with x/T + max(g) < L cannot win, so Philox and the logarithms are
+// skipped for it. Surviving 4-element groups are compacted across the warp, so
+// all 32 lanes run Philox on useful work, four independent calls per lane at a
+// time. A cheap bound on g from the Philox word then rejects almost every
+// survivor before the two exact logarithms.
 #include <cstdint>
+#include <type_traits>
+
+#include <cuda_bf16.h>
 
 #include "gsample_internal.h"
 
 namespace gsample {
 namespace {
 
-constexpr int kVPT = 8;  // units per lane per tile
+#ifndef GSAMPLE_VPT
+#define GSAMPLE_VPT 8
+#endif
+#ifndef GSAMPLE_STAGES
+#define GSAMPLE_STAGES 3
+#endif
+#ifndef GSAMPLE_MIN_CTAS_PER_SM
+#define GSAMPLE_MIN_CTAS_PER_SM 2
+#endif
+constexpr int kVPT = GSAMPLE_VPT;        // units per lane per tile
+constexpr int kStages = GSAMPLE_STAGES;  // tiles per warp ring
 
 template <int DT, bool VEC>
 struct Cfg {
@@ -36,12 +56,14 @@ struct Cfg {
   static constexpr int kEPU = VEC ? 16 / kElt : 4;  // elements per unit
   static constexpr int kGPU = kEPU / 4;             // Philox groups per unit
   static constexpr int kTile = 32 * kVPT;           // units per warp tile
-  static constexpr int kCap = 32 * kVPT * kGPU;     // compaction entries per warp
-  // Unit registers hold binary32 bits (f32 rows, or any dtype on the 4-element
-  // scalar path) or raw 16-bit values (bf16/f16 on the 128-bit path).
+  static constexpr int kCap = kTile * kGPU;         // groups per tile
+  // Units in shared memory hold binary32 bits (f32 rows, or any dtype on the
+  // 4-element scalar path) or raw 16-bit values (bf16/f16 on the 128-bit path).
   static constexpr bool kF32Bits = DT == 0 || !VEC;
-  static constexpr int kGroupBytes = kF32Bits ? 16 : 8;
-  static constexpr size_t kSmem = (size_t)kWarps * kCap * (4 + kGroupBytes);
+  static constexpr int kTileBytes = kTile * 16;
+  static constexpr int kListBytes = ((kCap * (kF32Bits ? 8 : 4) + 15) / 16) * 16;
+  static constexpr int kWarpBytes = kStages * kTileBytes + kListBytes;
+  static constexpr size_t kSmem = (size_t)kWarps * kWarpBytes;
 };
 
 template <int DT>
@@ -49,7 +71,7 @@ __device__ __forceinline__ float half_to_f32(uint32_t h) {
   return DT == 1 ? bf16_bits_to_f32(h) : f16_bits_to_f32(h);
 }
 
-// Element e (0 <= e < kEPU) of a unit held in registers.
+// Element e (0 <= e < kEPU) of a unit.
 template <int DT, bool VEC>
 __device__ __forceinline__ float unit_elt(const uint4& r, int e) {
   if constexpr (Cfg<DT, VEC>::kF32Bits) {
@@ -69,11 +91,6 @@ __device__ __forceinline__ float load_elt(const char* row, int32_t i) {
   }
 }
 
-template <int DT>
-__device__ __forceinline__ uint32_t load_half_bits(const char* row, int32_t i) {
-  return __ldg(reinterpret_cast<const unsigned short*>(row) + i);
-}
-
 constexpr uint32_t kNegInfF32 = 0xFF800000u;
 template <int DT>
 __host__ __device__ constexpr uint32_t neg_inf_half() { return DT == 1 ? 0xFF80u : 0xFC00u; }
@@ -88,36 +105,117 @@ __device__ __forceinline__ uint4 empty_unit() {
   }
 }
 
-// Unit u of a row; elements at or past V read as -inf.
+// Unit u of a row read with plain loads; elements at or past V read as -inf.
 template <int DT, bool VEC>
-__device__ __forceinline__ uint4 load_unit(const char* row, int32_t u, int32_t V, uint64_t pol) {
+__device__ __forceinline__ uint4 load_unit_sync(const char* row, int32_t u, int32_t V) {
   using C = Cfg<DT, VEC>;
   const int32_t e0 = u * C::kEPU;
-  if constexpr (VEC) {
-    if (e0 + C::kEPU <= V) return ld_stream_v4(row + (size_t)u * 16, pol);
-  }
   uint32_t w[4];
   if constexpr (C::kF32Bits) {
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       w[e] = (e0 + e < V) ? __float_as_uint(load_elt<DT>(row, e0 + e)) : kNegInfF32;
   } else {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = (e0 + 2 * k < V) ? load_half_bits<DT>(row, e0 + 2 * k) : neg_inf_half<DT>();
-      const uint32_t hi = (e0 + 2 * k + 1 < V) ? load_half_bits<DT>(row, e0 + 2 * k + 1) : neg_inf_half<DT>();
+      const uint32_t lo = (e0 + 2 * k < V) ? (uint32_t)__ldg(h + e0 + 2 * k) : neg_inf_half<DT>();
+      const uint32_t hi = (e0 + 2 * k + 1 < V) ? (uint32_t)__ldg(h + e0 + 2 * k + 1) : neg_inf_half<DT>();
       w[k] = lo | (hi << 16);
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ---------------------------------------------------------------------------
+// Shared-memory and cp.async primitives.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Packed 16-bit helpers: max of two bf16x2/f16x2 words and "any half >= thr".
+// The max ignores a NaN operand (like fmaxf); the compare is ordered (NaN false).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ uint32_t hmax2_bits(uint32_t a, uint32_t b) {
+  if constexpr (DT == 1) {
+    __nv_bfloat162 m = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&m);
+  } else {
+    __half2 m = __hmax2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&m);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ bool hge2_any(uint32_t a, uint32_t thr2) {
+  if constexpr (DT == 1) {
+    return __hge2_mask(*reinterpret_cast<__nv_bfloat162*>(&a),
+                       *reinterpret_cast<__nv_bfloat162*>(&thr2)) != 0u;
+  } else {
+    return __hge2_mask(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&thr2)) != 0u;
+  }
+}
+
+// thr rounded down to the 16-bit type, in both halves: x >= thr implies
+// x16 >= thr16, so the packed test never drops a survivor.
+template <int DT>
+__device__ __forceinline__ uint32_t packed_threshold(float thr) {
+  uint32_t h;
+  if constexpr (DT == 1) {
+    __nv_bfloat16 b = __float2bfloat16_rd(thr);
+    h = *reinterpret_cast<unsigned short*>(&b);
+  } else {
+    __half b = __float2half_rd(thr);
+    h = *reinterpret_cast<unsigned short*>(&b);
+  }
+  return h * 0x10001u;
+}
+
 template <int DT, bool VEC>
 __device__ __forceinline__ float unit_max(const uint4& r) {
-  float m = unit_elt<DT, VEC>(r, 0);
-#pragma unroll
-  for (int e = 1; e < Cfg<DT, VEC>::kEPU; ++e) m = fmaxf(m, unit_elt<DT, VEC>(r, e));
-  return m;  // fmaxf ignores NaN unless every element is NaN
+  if constexpr (Cfg<DT, VEC>::kF32Bits) {
+    return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                 fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+  } else {
+    const uint32_t m = hmax2_bits<DT>(hmax2_bits<DT>(r.x, r.y), hmax2_bits<DT>(r.z, r.w));
+    return fmaxf(half_to_f32<DT>(m & 0xFFFFu), half_to_f32<DT>(m >> 16));
+  }  // NaN is ignored unless every element is NaN
 }
 
 // Greedy: running (max, lowest index) over this lane's units, in index order.
@@ -136,231 +234,386 @@ __device__ __forceinline__ void greedy_unit(const uint4& r, int32_t u, float& bs
 }
 
 struct RowCtx {
-  const char* row;
-  int32_t V;
-  uint32_t row_id;
   float T;
   float rT;
-  uint32_t k0, k1;      // Philox key
-  uint32_t off0, off1;  // Philox counter words 2, 3
+  PhiloxRow ph;  // the row's Philox key and counter words, first rounds folded
   WsRow* ws;
 };
+
+__device__ __forceinline__ RowCtx row_context(const SampleParams& p, int64_t b) {
+  RowCtx rc;
+  rc.ws = p.ws + b;
+  rc.T = p.temperature ? __ldg(p.temperature + b) : 0.0f;
+  rc.rT = 1.0f;
+  rc.ph = PhiloxRow{0u, 0u, 0u, 0u, 0u, 0u};
+  if (rc.T > 0.0f) {  // NaN and T <= 0: greedy
+    const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
+    rc.ph = philox_row((uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32), (uint32_t)sd,
+                       (uint32_t)(sd >> 32));
+    rc.rT = 1.0f / rc.T;
+  }
+  return rc;
+}
 
 __device__ __forceinline__ float exact_score(float x, uint32_t word, float T) {
   return x == INFINITY ? INFINITY : __fdiv_rn(x, T) + gumbel_of_word(word);
 }
 
-// Publish the warp's best into the row key and return the row's best known
-// score (warp-uniform).
-__device__ __forceinline__ float publish_and_bound(WsRow* ws, float bs, int32_t bi, int lane) {
-  warp_argmax(bs, bi);
-  unsigned long long old = 0ull;
-  if (lane == 0) {
-    if (bi != INT32_MAX && bs > -INFINITY)
-      old = atomicMax(&ws->key, pack_key(bs, bi));
-    else
-      old = __ldcg(&ws->key);
+// Rare path: the element-wise test, then the exact score.
+__device__ __noinline__ void score_group(uint32_t gid, float x0, float x1, float x2, float x3,
+                                         uint4 w, Prune pr, ReachTest rt, float T, float* bs_io,
+                                         int32_t* bi_io) {
+  const float x[4] = {x0, x1, x2, x3};
+  float bs = *bs_io;
+  int32_t bi = *bi_io;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t wd = word_of(w, t);
+    const bool need = pr.use_bound ? may_reach(x[t], wd, rt) : (x[t] >= pr.thr_x);
+    if (need) take_better(exact_score(x[t], wd, T), (int32_t)(4 * gid + t), bs, bi);
   }
-  old = __shfl_sync(0xFFFFFFFFu, old, 0);
-  return fmaxf(bs, score_of_key(old));
+  *bs_io = bs;
+  *bi_io = bi;
 }
 
+// The four logits of tile-local group q (q = unit-in-tile * kGPU + h).
 template <int DT, bool VEC>
-__device__ void sample_segment(const RowCtx& rc, int32_t w_lo, int32_t w_hi, uint64_t pol,
-                               uint32_t* buf_gid, unsigned char* buf_data, float& bs,
-                               int32_t& bi) {
+__device__ __forceinline__ void group_values(uint32_t stage, uint32_t q, float x[4]) {
   using C = Cfg<DT, VEC>;
+  if constexpr (C::kF32Bits) {
+    const uint4 d = lds128(stage + q * 16u);
+    x[0] = __uint_as_float(d.x);
+    x[1] = __uint_as_float(d.y);
+    x[2] = __uint_as_float(d.z);
+    x[3] = __uint_as_float(d.w);
+  } else {
+    const uint2 d = lds64(stage + q * 8u);  // kGPU == 2: unit q/2, half q%2
+    x[0] = half_to_f32<DT>(d.x & 0xFFFFu);
+    x[1] = half_to_f32<DT>(d.x >> 16);
+    x[2] = half_to_f32<DT>(d.y & 0xFFFFu);
+    x[3] = half_to_f32<DT>(d.y >> 16);
+  }
+}
+
+// A list entry: tile-local group index q and the group's largest logit. 16-bit
+// inputs pack both in one word (q low, the 16-bit maximum high); binary32 needs
+// two words.
+template <int DT, bool VEC>
+struct ListEntry {
+  using T = typename std::conditional<Cfg<DT, VEC>::kF32Bits, uint2, uint32_t>::type;
+};
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void decode_entry(const typename ListEntry<DT, VEC>::T& e, uint32_t& q,
+                                             float& xm) {
+  if constexpr (Cfg<DT, VEC>::kF32Bits) {
+    q = e.x;
+    xm = __uint_as_float(e.y);
+  } else {
+    q = e & 0xFFFFu;
+    xm = half_to_f32<DT>(e >> 16);
+  }
+}
+
+// Can the group still reach L, given its largest logit and largest Philox word
+// (v = 1 - u only shrinks as the word grows, so one test covers all four)?
+__device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const Prune& pr,
+                                                const ReachTest& rt) {
+  if (!pr.use_bound) return xm >= pr.thr_x;
+  return may_reach(xm, max(max(w.x, w.y), max(w.z, w.w)), rt);
+}
+
+// Phase C: the tile's surviving groups, four per lane at a time so that a lane
+// keeps four independent Philox chains in flight.
+template <int DT, bool VEC>
+__device__ __forceinline__ void phase_c(uint32_t stage, const typename ListEntry<DT, VEC>::T* list,
+                                        int cnt, uint32_t g0, const RowCtx& rc, const Prune& pr,
+                                        float& bs, int32_t& bi) {
   const int lane = threadIdx.x & 31;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  uint4 r[kVPT];
-
-  auto load_tile = [&](int32_t t0) {
+  const ReachTest rt = make_reach(pr, rc.rT);
+  const int full = cnt & ~127;
+  for (int pa = lane; pa < full; pa += 128) {
+    uint32_t q[4], g[4];
+    float xm[4];
 #pragma unroll
-    for (int k = 0; k < kVPT; ++k) {
-      const int32_t u = t0 + k * 32 + lane;
-      r[k] = (u < w_hi) ? load_unit<DT, VEC>(rc.row, u, rc.V, pol) : empty_unit<DT, VEC>();
+    for (int j = 0; j < 4; ++j) {
+      decode_entry<DT, VEC>(list[pa + 32 * j], q[j], xm[j]);
+      g[j] = g0 + q[j];
     }
-  };
-
-  if (w_lo >= w_hi) return;
-  load_tile(w_lo);
-  bool first = true;
-  for (int32_t t0 = w_lo; t0 < w_hi; t0 += C::kTile) {
-    if (first) {
-      // Phase A: each lane scores its largest logit exactly -> a first L.
-      float cm = -INFINITY;
-      int ck = -1;
+    uint4 w[4];
+    philox_row_x4(g, rc.ph, w);
+    // All four tests first, branch-free; the exact path is rare.
+    uint32_t need = 0;
 #pragma unroll
-      for (int k = 0; k < kVPT; ++k) {
-        const float m = unit_max<DT, VEC>(r[k]);
-        if (m > cm) {
-          cm = m;
-          ck = k;
+    for (int j = 0; j < 4; ++j) need |= group_may_reach(xm[j], w[j], pr, rt) ? (1u << j) : 0u;
+    if (need) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (need & (1u << j)) {
+          float x[4];
+          group_values<DT, VEC>(stage, q[j], x);
+          score_group(g[j], x[0], x[1], x[2], x[3], w[j], pr, rt, rc.T, &bs, &bi);
         }
       }
-      if (ck >= 0) {
-        uint4 ru = r[0];
-#pragma unroll
-        for (int k = 1; k < kVPT; ++k)
-          if (k == ck) ru = r[k];
-        int ce = C::kEPU - 1;
-#pragma unroll
-        for (int e = C::kEPU - 1; e >= 0; --e)
-          if (unit_elt<DT, VEC>(ru, e) == cm) ce = e;
-        const int32_t i = (t0 + ck * 32 + lane) * C::kEPU + ce;
-        const uint4 blk = philox4x32_10(make_uint4((uint32_t)i >> 2, rc.row_id, rc.off0, rc.off1),
-                                        rc.k0, rc.k1);
-        take_better(exact_score(cm, word_of(blk, i & 3), rc.T), i, bs, bi);
-      }
-      first = false;
     }
-    const float L = publish_and_bound(rc.ws, bs, bi, lane);
-    const Prune pr = make_prune(L, rc.T);
-
-    // Phase B: append every group that may still win to the warp's buffer.
-    int cnt = 0;
-#pragma unroll
-    for (int k = 0; k < kVPT; ++k) {
-      const int32_t u = t0 + k * 32 + lane;
-#pragma unroll
-      for (int h = 0; h < C::kGPU; ++h) {
-        float gm = unit_elt<DT, VEC>(r[k], 4 * h);
-#pragma unroll
-        for (int e = 1; e < 4; ++e) gm = fmaxf(gm, unit_elt<DT, VEC>(r[k], 4 * h + e));
-        const bool keep = gm >= pr.thr_x;
-        const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
-        if (keep) {
-          const int pos = cnt + __popc(mask & lt_mask);
-          buf_gid[pos] = (uint32_t)(u * C::kGPU + h);
-          if constexpr (C::kF32Bits) {
-            reinterpret_cast<uint4*>(buf_data)[pos] = r[k];
-          } else {
-            reinterpret_cast<uint2*>(buf_data)[pos] =
-                h == 0 ? make_uint2(r[k].x, r[k].y) : make_uint2(r[k].z, r[k].w);
-          }
-        }
-        cnt += __popc(mask);
-      }
-    }
-    __syncwarp();
-
-    // Start the next tile's loads before the arithmetic on this one.
-    if (t0 + C::kTile < w_hi) load_tile(t0 + C::kTile);
-
-    // Phase C: exact scores of the surviving groups, one group per lane.
-    for (int p = lane; p < cnt; p += 32) {
-      const uint32_t gid = buf_gid[p];
+  }
+  for (int pa = full + lane; pa < cnt; pa += 32) {
+    uint32_t q;
+    float xm;
+    decode_entry<DT, VEC>(list[pa], q, xm);
+    const uint32_t g = g0 + q;
+    const uint4 w = philox_row_1(g, rc.ph);
+    if (group_may_reach(xm, w, pr, rt)) {
       float x[4];
-      if constexpr (C::kF32Bits) {
-        const uint4 d = reinterpret_cast<const uint4*>(buf_data)[p];
-        x[0] = __uint_as_float(d.x);
-        x[1] = __uint_as_float(d.y);
-        x[2] = __uint_as_float(d.z);
-        x[3] = __uint_as_float(d.w);
-      } else {
-        const uint2 d = reinterpret_cast<const uint2*>(buf_data)[p];
-        x[0] = half_to_f32<DT>(d.x & 0xFFFFu);
-        x[1] = half_to_f32<DT>(d.x >> 16);
-        x[2] = half_to_f32<DT>(d.y & 0xFFFFu);
-        x[3] = half_to_f32<DT>(d.y >> 16);
-      }
-      const uint4 blk = philox4x32_10(make_uint4(gid, rc.row_id, rc.off0, rc.off1), rc.k0, rc.k1);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float xv = x[t];
-        if (!(xv >= pr.thr_x)) continue;
-        const uint32_t wd = word_of(blk, t);
-        if (pr.use_bound && xv * rc.rT + gumbel_bound_of_word(wd) < pr.lm) continue;
-        take_better(exact_score(xv, wd, rc.T), (int32_t)(4 * gid + t), bs, bi);
-      }
+      group_values<DT, VEC>(stage, q, x);
+      score_group(g, x[0], x[1], x[2], x[3], w, pr, rt, rc.T, &bs, &bi);
     }
-    __syncwarp();
   }
 }
 
+// Phase A: this lane's largest logit of the tile, scored exactly.
 template <int DT, bool VEC>
-__device__ void greedy_segment(const RowCtx& rc, int32_t w_lo, int32_t w_hi, uint64_t pol,
-                               float& bs, int32_t& bi) {
+__device__ __forceinline__ void lane_candidate(uint32_t stage, int32_t t0, int32_t t_hi,
+                                               const RowCtx& rc, float& bs, int32_t& bi) {
   using C = Cfg<DT, VEC>;
   const int lane = threadIdx.x & 31;
-  for (int32_t t0 = w_lo; t0 < w_hi; t0 += C::kTile) {
-    uint4 r[kVPT];
+  float cm = -INFINITY;
+  int ck = -1;
 #pragma unroll
-    for (int k = 0; k < kVPT; ++k) {
-      const int32_t u = t0 + k * 32 + lane;
-      r[k] = (u < w_hi) ? load_unit<DT, VEC>(rc.row, u, rc.V, pol) : empty_unit<DT, VEC>();
+  for (int k = 0; k < kVPT; ++k) {
+    if (t0 + k * 32 + lane >= t_hi) break;
+    const float m = unit_max<DT, VEC>(lds128(stage + (uint32_t)(k * 32 + lane) * 16u));
+    if (m > cm) {
+      cm = m;
+      ck = k;
     }
-#pragma unroll
-    for (int k = 0; k < kVPT; ++k) greedy_unit<DT, VEC>(r[k], t0 + k * 32 + lane, bs, bi);
   }
+  if (ck < 0) return;
+  const uint4 ru = lds128(stage + (uint32_t)(ck * 32 + lane) * 16u);
+  int ce = C::kEPU - 1;
+#pragma unroll
+  for (int e = C::kEPU - 1; e >= 0; --e)
+    if (unit_elt<DT, VEC>(ru, e) == cm) ce = e;
+  const int32_t i = (t0 + ck * 32 + lane) * C::kEPU + ce;
+  const uint4 blk = philox_row_1((uint32_t)i >> 2, rc.ph);
+  take_better(exact_score(cm, word_of(blk, i & 3), rc.T), i, bs, bi);
 }
 
-// First unit of the CTA range that holds unit u (balanced split of U units
-// over G CTAs: the first U % G CTAs take one unit more).
-__device__ __forceinline__ int64_t owner_cta(int64_t u, int64_t U, int64_t G) {
-  const int64_t base = U / G, rem = U % G;
+// Warp-uniform cursor over this warp's tiles: row b, row-local units
+// [t0, t_hi), and the end of the warp's part of row b (seg_hi).
+struct TileCursor {
+  int64_t b;
+  int32_t t0, t_hi, seg_hi;
+  bool valid;
+};
+
+template <int TILE>
+__device__ __forceinline__ TileCursor first_tile(int64_t u_begin, int64_t u_end, int64_t NU) {
+  TileCursor c;
+  c.b = u_begin / NU;
+  c.t0 = (int32_t)(u_begin - c.b * NU);
+  c.seg_hi = (int32_t)((u_end < (c.b + 1) * NU ? u_end : (c.b + 1) * NU) - c.b * NU);
+  c.t_hi = min(c.t0 + TILE, c.seg_hi);
+  c.valid = u_begin < u_end;
+  return c;
+}
+
+template <int TILE>
+__device__ __forceinline__ TileCursor next_tile(const TileCursor& c, int64_t u_end, int64_t NU) {
+  TileCursor n = c;
+  if (!c.valid) return n;
+  if (c.t_hi < c.seg_hi) {
+    n.t0 = c.t_hi;
+  } else {
+    n.b = c.b + 1;
+    n.t0 = 0;
+    n.valid = n.b * NU < u_end;
+    n.seg_hi = n.valid ? (int32_t)((u_end < (n.b + 1) * NU ? u_end : (n.b + 1) * NU) - n.b * NU) : 0;
+  }
+  n.t_hi = min(n.t0 + TILE, n.seg_hi);
+  return n;
+}
+
+// Start copying a tile into a ring stage and close its cp.async group (an empty
+// group when there is no tile, so that group counting stays uniform). Units
+// past the tile, and elements past V in a row's last unit, read as -inf.
+template <int DT, bool VEC>
+__device__ __forceinline__ void issue_tile(const SampleParams& p, const TileCursor& c,
+                                           uint32_t stage, uint64_t pol) {
+  using C = Cfg<DT, VEC>;
+  if (c.valid) {
+    const int lane = threadIdx.x & 31;
+    const char* row = p.logits + c.b * p.ld_bytes;
+    if (VEC && c.t_hi - c.t0 == C::kTile && c.t_hi * C::kEPU <= p.V) {
+      // A full tile inside the row: kVPT coalesced 512-byte copies, no checks.
+      const char* src = row + (size_t)(c.t0 + lane) * 16;
+      const uint32_t dst = stage + (uint32_t)lane * 16u;
+#pragma unroll
+      for (int k = 0; k < kVPT; ++k) cp_async16(dst + k * 512u, src + k * 512, pol);
+      cp_async_commit();
+      return;
+    }
+#pragma unroll
+    for (int k = 0; k < kVPT; ++k) {
+      const int32_t u = c.t0 + k * 32 + lane;
+      const uint32_t dst = stage + (uint32_t)(k * 32 + lane) * 16u;
+      if (VEC && u < c.t_hi && (u + 1) * C::kEPU <= p.V) {
+        cp_async16(dst, row + (size_t)u * 16, pol);
+      } else if (u < c.t_hi) {
+        sts128(dst, load_unit_sync<DT, VEC>(row, u, p.V));
+      } else {
+        sts128(dst, empty_unit<DT, VEC>());
+      }
+    }
+  }
+  cp_async_commit();
+}
+
+// Index of the warp whose range holds unit u, for U units dealt to NW warps in
+// near-equal contiguous ranges (the first U % NW warps take one unit more).
+__device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t U, int64_t NW) {
+  const int64_t base = U / NW, rem = U % NW;
   const int64_t big = rem * (base + 1);
   return u < big ? u / (base + 1) : rem + (u - big) / base;
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) {
+__global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kernel(const SampleParams p) {
   using C = Cfg<DT, VEC>;
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  uint32_t* buf_gid = reinterpret_cast<uint32_t*>(smem) + warp * C::kCap;
-  unsigned char* buf_data = smem + (size_t)kWarps * C::kCap * 4 + (size_t)warp * C::kCap * C::kGroupBytes;
+  unsigned char* wbase = smem + (size_t)warp * C::kWarpBytes;
+  const uint32_t ring = smem_addr(wbase);
+  using Entry = typename ListEntry<DT, VEC>::T;
+  Entry* list = reinterpret_cast<Entry*>(wbase + kStages * C::kTileBytes);
   const uint64_t pol = evict_first_policy();
 
-  const int64_t U = p.total_units, G = p.ctas, NU = p.units_per_row;
-  const int64_t c = blockIdx.x;
-  const int64_t base = U / G, rem = U % G;
-  const int64_t u_begin = c * base + (c < rem ? c : rem);
-  const int64_t u_end = u_begin + base + (c < rem ? 1 : 0);
+  const int64_t U = p.total_units, NU = p.units_per_row, NW = p.warps;
+  const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+  if (gw >= NW) return;
+  const int64_t base = U / NW, rem = U % NW;
+  const int64_t u_begin = gw * base + (gw < rem ? gw : rem);
+  const int64_t u_end = u_begin + base + (gw < rem ? 1 : 0);
 
-  for (int64_t b = u_begin / NU; b * NU < u_end; ++b) {
-    const int64_t row_u0 = b * NU;
-    const int32_t lo = (int32_t)((u_begin > row_u0 ? u_begin : row_u0) - row_u0);
-    const int32_t hi = (int32_t)((u_end < row_u0 + NU ? u_end : row_u0 + NU) - row_u0);
-    const int32_t n = hi - lo;
-    const int32_t w_lo = lo + (int32_t)((int64_t)n * warp / kWarps);
-    const int32_t w_hi = lo + (int32_t)((int64_t)n * (warp + 1) / kWarps);
+  // Prologue: the first kStages - 1 tiles go in flight.
+  TileCursor cur = first_tile<C::kTile>(u_begin, u_end, NU);
+  TileCursor ahead = cur;
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    issue_tile<DT, VEC>(p, ahead, ring + s * C::kTileBytes, pol);
+    ahead = next_tile<C::kTile>(ahead, u_end, NU);
+  }
 
-    RowCtx rc;
-    rc.row = p.logits + b * p.ld_bytes;
-    rc.V = p.V;
-    rc.row_id = (uint32_t)b;
-    rc.ws = p.ws + b;
-    rc.T = p.temperature ? __ldg(p.temperature + b) : 0.0f;
-    float bs = -INFINITY;
-    int32_t bi = INT32_MAX;
-    if (rc.T > 0.0f) {  // NaN and T <= 0: greedy
-      const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
-      rc.k0 = (uint32_t)sd;
-      rc.k1 = (uint32_t)(sd >> 32);
-      rc.off0 = (uint32_t)of;
-      rc.off1 = (uint32_t)(of >> 32);
-      rc.rT = 1.0f / rc.T;
-      sample_segment<DT, VEC>(rc, w_lo, w_hi, pol, buf_gid, buf_data, bs, bi);
+  RowCtx rc = row_context(p, cur.b);
+  bool seg_first = true;
+  float bs = -INFINITY;
+  int32_t bi = INT32_MAX;
+  // The row key, read one tile ahead of its use so that the load's latency
+  // hides behind a tile of work; `seen` is the value being used now.
+  unsigned long long seen = 0ull, pending = 0ull;
+  int slot = 0;
+
+  while (true) {
+    // The current tile has landed (this lane's copies, then everyone's).
+    cp_async_wait<kStages - 2>();
+    __syncwarp();
+    const uint32_t stage = ring + slot * C::kTileBytes;
+    // Refill the ring slot that the previous tile freed.
+    int fill = slot + kStages - 1;
+    if (fill >= kStages) fill -= kStages;
+    issue_tile<DT, VEC>(p, ahead, ring + fill * C::kTileBytes, pol);
+    ahead = next_tile<C::kTile>(ahead, u_end, NU);
+
+    const int32_t t0 = cur.t0, t_hi = cur.t_hi;
+    if (rc.T > 0.0f) {
+      if (seg_first) {
+        lane_candidate<DT, VEC>(stage, t0, t_hi, rc, bs, bi);
+        seen = 0ull;
+      } else {
+        seen = pending;
+      }
+      pending = __ldcg(&rc.ws->key);
+      // One warp reduction gives both the key to publish (fire-and-forget)
+      // and the bound L for this tile.
+      unsigned long long wk = (bi != INT32_MAX && bs > -INFINITY) ? pack_key(bs, bi) : 0ull;
+      wk = warp_max_u64(wk);
+      if (lane == 0 && wk > seen) atomicMax(&rc.ws->key, wk);
+      const float L = score_of_key(wk > seen ? wk : seen);
+      const Prune pr = make_prune(L, rc.T);
+      uint32_t thr2 = 0;
+      if constexpr (!C::kF32Bits) thr2 = packed_threshold<DT>(pr.thr_x);
+
+      // Phase B: list the groups of the tile that may still win.
+      int cnt = 0;
+      const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+      for (int k = 0; k < kVPT; ++k) {
+        const uint4 r = lds128(stage + (uint32_t)(k * 32 + lane) * 16u);
+#pragma unroll
+        for (int h = 0; h < C::kGPU; ++h) {
+          const uint32_t q = (uint32_t)((k * 32 + lane) * C::kGPU + h);
+          if constexpr (C::kF32Bits) {
+            const float gm = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                                   fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+            const bool keep = gm >= pr.thr_x;
+            const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
+            if (keep) list[cnt + __popc(mask & lt_mask)] = make_uint2(q, __float_as_uint(gm));
+            cnt += __popc(mask);
+          } else {
+            const uint32_t m2 = h == 0 ? hmax2_bits<DT>(r.x, r.y) : hmax2_bits<DT>(r.z, r.w);
+            const bool keep = hge2_any<DT>(m2, thr2);
+            const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
+            if (keep) {
+              // the larger half of the pair, as a 16-bit value, next to q
+              const uint32_t mm = hmax2_bits<DT>(m2, __funnelshift_l(m2, m2, 16));
+              list[cnt + __popc(mask & lt_mask)] = q | (mm << 16);
+            }
+            cnt += __popc(mask);
+          }
+        }
+      }
+      __syncwarp();
+      phase_c<DT, VEC>(stage, list, cnt, (uint32_t)t0 * C::kGPU, rc, pr, bs, bi);
     } else {
-      greedy_segment<DT, VEC>(rc, w_lo, w_hi, pol, bs, bi);
-    }
-    warp_argmax(bs, bi);
-    if (lane == 0 && bi != INT32_MAX && bs > -INFINITY) atomicMax(&rc.ws->key, pack_key(bs, bi));
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int64_t expected = owner_cta(row_u0 + NU - 1, U, G) - owner_cta(row_u0, U, G) + 1;
-      const unsigned t = atomicAdd(&rc.ws->ticket, 1u);
-      if ((int64_t)t == expected - 1) {
-        __threadfence();
-        const unsigned long long key = atomicExch(&rc.ws->key, 0ull);
-        atomicExch(&rc.ws->ticket, 0u);
-        p.out_idx[b] = index_of_key(key);
+#pragma unroll
+      for (int k = 0; k < kVPT; ++k) {
+        const int32_t u = t0 + k * 32 + lane;
+        greedy_unit<DT, VEC>(lds128(stage + (uint32_t)(k * 32 + lane) * 16u), u, bs, bi);
       }
     }
+    __syncwarp();  // every lane is done with this stage before it is refilled
+
+    if (cur.t_hi == cur.seg_hi) {
+      // This warp's part of row b is done: merge it, then count it in the
+      // row's ticket; the warp that completes the count writes the answer.
+      warp_argmax(bs, bi);
+      if (lane == 0) {
+        if (bi != INT32_MAX && bs > -INFINITY) atomicMax(&rc.ws->key, pack_key(bs, bi));
+        __threadfence();
+        const int64_t expected =
+            owner_warp(cur.b * NU + NU - 1, U, NW) - owner_warp(cur.b * NU, U, NW) + 1;
+        const unsigned t = atomicAdd(&rc.ws->ticket, 1u);
+        if ((int64_t)t == expected - 1) {
+          __threadfence();
+          const unsigned long long key = atomicExch(&rc.ws->key, 0ull);
+          atomicExch(&rc.ws->ticket, 0u);
+          p.out_idx[cur.b] = index_of_key(key);
+        }
+      }
+      cur = next_tile<C::kTile>(cur, u_end, NU);
+      if (!cur.valid) break;
+      rc = row_context(p, cur.b);
+      bs = -INFINITY;
+      bi = INT32_MAX;
+      seg_first = true;
+    } else {
+      cur = next_tile<C::kTile>(cur, u_end, NU);
+      seg_first = false;
+    }
+    slot = slot + 1 == kStages ? 0 : slot + 1;
   }
+  cp_async_wait<0>();  // no copy may outlive the warp
 }
 
 template <int DT, bool VEC>
