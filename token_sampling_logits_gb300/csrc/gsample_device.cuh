@@ -17,14 +17,16 @@ namespace gsample {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 
-// Per-row cross-CTA merge state (16 bytes). `key` holds the best packed
-// (score, index) seen so far; `ticket` counts CTAs that finished the row. The
-// last CTA of a row writes the result and zeroes both, so a workspace is left
-// clean after every launch.
+// Per-row merge state (16 bytes). `key` holds the best packed (score, index)
+// merged so far; `ticket` counts the units of the row already finished (the
+// sampler) or the CTAs that finished it (the HLG kernel); `hint` holds the
+// order-preserving bits of the best score any warp has published for pruning.
+// Whoever completes a row writes its result and zeroes all three, so a
+// workspace is left clean after every launch.
 struct WsRow {
   unsigned long long key;
   unsigned int ticket;
-  unsigned int reserved;
+  unsigned int hint;
 };
 static_assert(sizeof(WsRow) == 16, "workspace row is 16 bytes");
 

@@ -24,10 +24,13 @@
 // Exact pruning (sampled rows). Each warp keeps L, the best exact score known
 // for the row (its own candidates and whatever other warps have published). An
 // element with x/T + max(g) < L cannot win, so Philox and the logarithms are
-// skipped for it. Surviving 4-element groups are compacted across the warp, so
-// all 32 lanes run Philox on useful work, four independent calls per lane at a
-// time. A cheap bound on g from the Philox word then rejects almost every
-// survivor before the two exact logarithms.
+// skipped for it: a tile whose logits all sit below L - max(g) is skipped
+// whole. In the other tiles every 4-element group gets its Philox block, four
+// independent blocks per lane at a time, and a cheap bound on g from the
+// largest word of the block rejects almost every group before the two exact
+// logarithms. The few survivors wait in a per-warp list and are scored 32 at a
+// time, one per lane. (A compaction variant, GSAMPLE_COMPACT, lists the groups
+// that pass the logit threshold and runs Philox only on those.)
 #include <cstdint>
 #include <type_traits>
 
@@ -46,6 +49,9 @@ namespace {
 #endif
 #ifndef GSAMPLE_MIN_CTAS_PER_SM
 #define GSAMPLE_MIN_CTAS_PER_SM 2
+#endif
+#ifndef GSAMPLE_COMPACT
+#define GSAMPLE_COMPACT 0
 #endif
 constexpr int kVPT = GSAMPLE_VPT;        // units per lane per tile
 constexpr int kStages = GSAMPLE_STAGES;  // tiles per warp ring
@@ -255,12 +261,56 @@ __device__ __forceinline__ RowCtx row_context(const SampleParams& p, int64_t b) 
   return rc;
 }
 
+// A row's raw parameters, loaded ahead of use (zeros past the last row).
+struct RowParams {
+  float T;
+  uint64_t seed, offset;
+};
+
+__device__ __forceinline__ RowParams load_row_params(const SampleParams& p, int64_t b) {
+  RowParams r{0.0f, 0ull, 0ull};
+  if (b < p.B && p.temperature) {
+    r.T = __ldg(p.temperature + b);
+    r.seed = __ldg(p.seed + b);
+    r.offset = __ldg(p.offset + b);
+  }
+  return r;
+}
+
+__device__ __forceinline__ RowCtx row_context_from(const SampleParams& p, int64_t b,
+                                                   const RowParams& r) {
+  RowCtx rc;
+  rc.ws = p.ws + b;
+  rc.T = r.T;
+  rc.rT = 1.0f;
+  rc.ph = PhiloxRow{0u, 0u, 0u, 0u, 0u, 0u};
+  if (rc.T > 0.0f) {
+    rc.ph = philox_row((uint32_t)b, (uint32_t)r.offset, (uint32_t)(r.offset >> 32),
+                       (uint32_t)r.seed, (uint32_t)(r.seed >> 32));
+    rc.rT = 1.0f / rc.T;
+  }
+  return rc;
+}
+
+// The warp whose ticket brought the row's finished-unit count to NU writes the
+// row's answer and clears its workspace slot.
+__device__ __noinline__ void finish_row_if_last(const SampleParams& p, int64_t b, uint32_t before,
+                                                uint32_t mine, int64_t NU) {
+  if ((int64_t)before + mine != NU) return;
+  WsRow* ws = p.ws + b;
+  __threadfence();
+  const unsigned long long key = atomicExch(&ws->key, 0ull);
+  atomicExch(&ws->ticket, 0u);
+  atomicExch(&ws->hint, 0u);
+  p.out_idx[b] = index_of_key(key);
+}
+
 __device__ __forceinline__ float exact_score(float x, uint32_t word, float T) {
   return x == INFINITY ? INFINITY : __fdiv_rn(x, T) + gumbel_of_word(word);
 }
 
 // Rare path: the element-wise test, then the exact score.
-__device__ __noinline__ void score_group(uint32_t gid, float x0, float x1, float x2, float x3,
+__device__ __forceinline__ void score_group(uint32_t gid, float x0, float x1, float x2, float x3,
                                          uint4 w, Prune pr, ReachTest rt, float T, float* bs_io,
                                          int32_t* bi_io) {
   const float x[4] = {x0, x1, x2, x3};
@@ -324,50 +374,196 @@ __device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const 
 }
 
 // Phase C: the tile's surviving groups, four per lane at a time so that a lane
-// keeps four independent Philox chains in flight.
+// keeps four independent Philox chains in flight. The few groups that pass the
+// group-level test are not scored on the spot (one lane would keep the other
+// 31 idle through two logarithms): their list entries are compacted into the
+// already-consumed front of the list and scored afterwards, one per lane.
 template <int DT, bool VEC>
-__device__ __forceinline__ void phase_c(uint32_t stage, const typename ListEntry<DT, VEC>::T* list,
+__device__ __forceinline__ void phase_c(uint32_t stage, typename ListEntry<DT, VEC>::T* list,
                                         int cnt, uint32_t g0, const RowCtx& rc, const Prune& pr,
                                         float& bs, int32_t& bi) {
+  using Entry = typename ListEntry<DT, VEC>::T;
   const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
   const ReachTest rt = make_reach(pr, rc.rT);
+  int rcnt = 0;  // deferred entries, stored in list[0, rcnt) (always <= entries read so far)
   const int full = cnt & ~127;
-  for (int pa = lane; pa < full; pa += 128) {
-    uint32_t q[4], g[4];
+  for (int base = 0; base < full; base += 128) {
+    Entry e[4];
+    uint32_t g[4];
     float xm[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      decode_entry<DT, VEC>(list[pa + 32 * j], q[j], xm[j]);
-      g[j] = g0 + q[j];
+      uint32_t q;
+      e[j] = list[base + lane + 32 * j];
+      decode_entry<DT, VEC>(e[j], q, xm[j]);
+      g[j] = g0 + q;
     }
     uint4 w[4];
     philox_row_x4(g, rc.ph, w);
-    // All four tests first, branch-free; the exact path is rare.
     uint32_t need = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) need |= group_may_reach(xm[j], w[j], pr, rt) ? (1u << j) : 0u;
-    if (need) {
+    if (__any_sync(0xFFFFFFFFu, need != 0u)) {
+      __syncwarp();  // every lane has read this round's entries
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (need & (1u << j)) {
-          float x[4];
-          group_values<DT, VEC>(stage, q[j], x);
-          score_group(g[j], x[0], x[1], x[2], x[3], w[j], pr, rt, rc.T, &bs, &bi);
-        }
+        const bool keep = (need >> j) & 1u;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+        if (keep) list[rcnt + __popc(m & lt_mask)] = e[j];
+        rcnt += __popc(m);
       }
     }
   }
-  for (int pa = full + lane; pa < cnt; pa += 32) {
+  for (int base = full; base < cnt; base += 32) {
+    const int pa = base + lane;
+    const bool valid = pa < cnt;
+    Entry e = valid ? list[pa] : Entry{};
     uint32_t q;
     float xm;
-    decode_entry<DT, VEC>(list[pa], q, xm);
+    decode_entry<DT, VEC>(e, q, xm);
+    const uint4 w = philox_row_1(g0 + q, rc.ph);
+    const bool keep = valid && group_may_reach(xm, w, pr, rt);
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+    if (m) {
+      __syncwarp();
+      if (keep) list[rcnt + __popc(m & lt_mask)] = e;
+      rcnt += __popc(m);
+    }
+  }
+  if (rcnt == 0) return;
+  __syncwarp();
+  for (int p = lane; p < rcnt; p += 32) {
+    uint32_t q;
+    float xm;
+    decode_entry<DT, VEC>(list[p], q, xm);
     const uint32_t g = g0 + q;
     const uint4 w = philox_row_1(g, rc.ph);
-    if (group_may_reach(xm, w, pr, rt)) {
-      float x[4];
-      group_values<DT, VEC>(stage, q, x);
-      score_group(g, x[0], x[1], x[2], x[3], w, pr, rt, rc.T, &bs, &bi);
+    float x[4];
+    group_values<DT, VEC>(stage, q, x);
+    score_group(g, x[0], x[1], x[2], x[3], w, pr, rt, rc.T, &bs, &bi);
+  }
+}
+
+// Groups that passed the cheap test wait in a per-warp list, across tiles,
+// until 32 of them (or the end of the warp's part of the row) make one exact
+// pass with every lane busy. An entry holds the row-local group index and the
+// group's four logits as stored in the tile (so the ring stage may be reused).
+constexpr int kRareCap = 32;
+constexpr uint32_t kRareRawOff = kRareCap * 4;  // byte offset of the logits array
+static_assert(kRareRawOff + kRareCap * 16 <= Cfg<0, true>::kListBytes &&
+                  kRareRawOff + kRareCap * 8 <= Cfg<1, true>::kListBytes,
+              "the rare list must fit in a warp's list area");
+
+template <int DT, bool VEC>
+using RareRaw = typename std::conditional<Cfg<DT, VEC>::kF32Bits, uint4, uint2>::type;
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void raw_values(const RareRaw<DT, VEC>& r, float x[4]) {
+  if constexpr (Cfg<DT, VEC>::kF32Bits) {
+    x[0] = __uint_as_float(r.x);
+    x[1] = __uint_as_float(r.y);
+    x[2] = __uint_as_float(r.z);
+    x[3] = __uint_as_float(r.w);
+  } else {
+    x[0] = half_to_f32<DT>(r.x & 0xFFFFu);
+    x[1] = half_to_f32<DT>(r.x >> 16);
+    x[2] = half_to_f32<DT>(r.y & 0xFFFFu);
+    x[3] = half_to_f32<DT>(r.y >> 16);
+  }
+}
+
+// Score the listed groups exactly (one per lane) against the current bound.
+template <int DT, bool VEC>
+__device__ __forceinline__ void flush_rare(const unsigned char* rbase, int rcnt, const RowCtx& rc,
+                                           const Prune& pr, float& bs, int32_t& bi) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();  // the entries of every lane are visible
+  if (lane < rcnt) {
+    const uint32_t g = reinterpret_cast<const uint32_t*>(rbase)[lane];
+    float x[4];
+    raw_values<DT, VEC>(reinterpret_cast<const RareRaw<DT, VEC>*>(rbase + kRareRawOff)[lane], x);
+    const uint4 w = philox_row_1(g, rc.ph);
+    score_group(g, x[0], x[1], x[2], x[3], w, pr, make_reach(pr, rc.rT), rc.T, &bs, &bi);
+  }
+  __syncwarp();  // every lane has read its entry before the list is refilled
+}
+
+// Tile-local group q of this lane's i-th group (unit i / kGPU, half i % kGPU).
+template <int DT, bool VEC>
+__device__ __forceinline__ uint32_t lane_group(int i, int lane) {
+  using C = Cfg<DT, VEC>;
+  return (uint32_t)(((i / C::kGPU) * 32 + lane) * C::kGPU + i % C::kGPU);
+}
+
+// Dense pass over a sampled tile, written as straight-line code so that the
+// shared-memory reads, the four-way Philox batches and the tests of different
+// batches can overlap. One vote skips the whole tile when no logit in it
+// reaches the logit threshold; otherwise every group of the tile gets its
+// Philox block and the word-level test, and the few survivors go to the rare
+// list.
+template <int DT, bool VEC>
+__device__ __forceinline__ void dense_tile(uint32_t stage, uint32_t g0, const RowCtx& rc,
+                                            const Prune& pr, unsigned char* rbase, int& rcnt,
+                                            float& bs, int32_t& bi) {
+  using C = Cfg<DT, VEC>;
+  constexpr int NG = kVPT * C::kGPU;  // groups per lane in a tile
+  static_assert(NG % 4 == 0, "groups per lane must fill four-way Philox batches");
+  const int lane = threadIdx.x & 31;
+  float xm[NG];
+#pragma unroll
+  for (int k = 0; k < kVPT; ++k) {
+    const uint4 r = lds128(stage + (uint32_t)(k * 32 + lane) * 16u);
+    if constexpr (C::kF32Bits) {
+      xm[k] = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                    fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+    } else {
+      const uint32_t m0 = hmax2_bits<DT>(r.x, r.y), m1 = hmax2_bits<DT>(r.z, r.w);
+      xm[2 * k] = fmaxf(half_to_f32<DT>(m0 & 0xFFFFu), half_to_f32<DT>(m0 >> 16));
+      xm[2 * k + 1] = fmaxf(half_to_f32<DT>(m1 & 0xFFFFu), half_to_f32<DT>(m1 >> 16));
     }
+  }
+  float tm = xm[0];
+#pragma unroll
+  for (int i = 1; i < NG; ++i) tm = fmaxf(tm, xm[i]);
+  if (!__any_sync(0xFFFFFFFFu, tm >= pr.thr_x)) return;  // nothing here can win
+
+  const ReachTest rt = make_reach(pr, rc.rT);
+  uint32_t need = 0;
+#pragma unroll
+  for (int b = 0; b < NG; b += 4) {
+    uint32_t g[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g[j] = g0 + lane_group<DT, VEC>(b + j, lane);
+    uint4 w[4];
+    philox_row_x4(g, rc.ph, w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      need |= group_may_reach(xm[b + j], w[j], pr, rt) ? (1u << (b + j)) : 0u;
+  }
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  while (__any_sync(0xFFFFFFFFu, need != 0u)) {
+    const bool has = need != 0u;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, has);
+    const int n = __popc(m);
+    if (rcnt + n > kRareCap) {
+      flush_rare<DT, VEC>(rbase, rcnt, rc, pr, bs, bi);
+      rcnt = 0;
+    }
+    if (has) {
+      const uint32_t q = lane_group<DT, VEC>(__ffs(need) - 1, lane);
+      need &= need - 1u;
+      const int s = rcnt + __popc(m & lt_mask);
+      reinterpret_cast<uint32_t*>(rbase)[s] = g0 + q;
+      auto* raw = reinterpret_cast<RareRaw<DT, VEC>*>(rbase + kRareRawOff);
+      if constexpr (C::kF32Bits) {
+        raw[s] = lds128(stage + q * 16u);
+      } else {
+        raw[s] = lds64(stage + q * 8u);
+      }
+    }
+    rcnt += n;
   }
 }
 
@@ -400,38 +596,41 @@ __device__ __forceinline__ void lane_candidate(uint32_t stage, int32_t t0, int32
 }
 
 // Warp-uniform cursor over this warp's tiles: row b, row-local units
-// [t0, t_hi), and the end of the warp's part of row b (seg_hi).
+// [t0, t_hi), and the warp's part of row b, [seg_lo, seg_hi).
 struct TileCursor {
   int64_t b;
-  int32_t t0, t_hi, seg_hi;
+  int32_t t0, t_hi, seg_lo, seg_hi;
   bool valid;
 };
 
-template <int TILE>
-__device__ __forceinline__ TileCursor first_tile(int64_t u_begin, int64_t u_end, int64_t NU) {
+__device__ __forceinline__ TileCursor segment_at(int64_t b, int64_t u_lo, int64_t u_end,
+                                                 int64_t NU, int tile) {
   TileCursor c;
-  c.b = u_begin / NU;
-  c.t0 = (int32_t)(u_begin - c.b * NU);
-  c.seg_hi = (int32_t)((u_end < (c.b + 1) * NU ? u_end : (c.b + 1) * NU) - c.b * NU);
-  c.t_hi = min(c.t0 + TILE, c.seg_hi);
-  c.valid = u_begin < u_end;
+  c.b = b;
+  c.valid = u_lo < u_end;
+  const int64_t row0 = b * NU;
+  c.seg_lo = (int32_t)(u_lo - row0);
+  c.seg_hi = c.valid ? (int32_t)((u_end < row0 + NU ? u_end : row0 + NU) - row0) : 0;
+  c.t0 = c.seg_lo;
+  c.t_hi = min(c.t0 + tile, c.seg_hi);
   return c;
+}
+
+// The first tile of the next row of this warp's range (rare: once per row).
+__device__ __noinline__ TileCursor next_row(int64_t b, int64_t u_end, int64_t NU, int tile) {
+  return segment_at(b + 1, (b + 1) * NU, u_end, NU, tile);
 }
 
 template <int TILE>
 __device__ __forceinline__ TileCursor next_tile(const TileCursor& c, int64_t u_end, int64_t NU) {
-  TileCursor n = c;
-  if (!c.valid) return n;
+  if (!c.valid) return c;
   if (c.t_hi < c.seg_hi) {
+    TileCursor n = c;
     n.t0 = c.t_hi;
-  } else {
-    n.b = c.b + 1;
-    n.t0 = 0;
-    n.valid = n.b * NU < u_end;
-    n.seg_hi = n.valid ? (int32_t)((u_end < (n.b + 1) * NU ? u_end : (n.b + 1) * NU) - n.b * NU) : 0;
+    n.t_hi = min(n.t0 + TILE, c.seg_hi);
+    return n;
   }
-  n.t_hi = min(n.t0 + TILE, n.seg_hi);
-  return n;
+  return next_row(c.b, u_end, NU, TILE);
 }
 
 // Start copying a tile into a ring stage and close its cp.async group (an empty
@@ -469,12 +668,16 @@ __device__ __forceinline__ void issue_tile(const SampleParams& p, const TileCurs
   cp_async_commit();
 }
 
-// Index of the warp whose range holds unit u, for U units dealt to NW warps in
-// near-equal contiguous ranges (the first U % NW warps take one unit more).
-__device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t U, int64_t NW) {
-  const int64_t base = U / NW, rem = U % NW;
-  const int64_t big = rem * (base + 1);
-  return u < big ? u / (base + 1) : rem + (u - big) / base;
+__device__ __forceinline__ float warp_max_f32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// The hint word holds the ordered bits of the best score any warp has seen in
+// the row so far (0: none yet).
+__device__ __forceinline__ float score_of_hint(uint32_t h) {
+  return h == 0u ? -INFINITY : score_of_key((unsigned long long)h << 32 | 1ull);
 }
 
 template <int DT, bool VEC>
@@ -497,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
   const int64_t u_end = u_begin + base + (gw < rem ? 1 : 0);
 
   // Prologue: the first kStages - 1 tiles go in flight.
-  TileCursor cur = first_tile<C::kTile>(u_begin, u_end, NU);
+  TileCursor cur = segment_at(u_begin / NU, u_begin, u_end, NU, C::kTile);
   TileCursor ahead = cur;
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
@@ -506,13 +709,25 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
   }
 
   RowCtx rc = row_context(p, cur.b);
+  // The next row's parameters, loaded a whole segment before they are needed.
+  RowParams next_params = load_row_params(p, cur.b + 1);
   bool seg_first = true;
   float bs = -INFINITY;
   int32_t bi = INT32_MAX;
-  // The row key, read one tile ahead of its use so that the load's latency
-  // hides behind a tile of work; `seen` is the value being used now.
-  unsigned long long seen = 0ull, pending = 0ull;
+  // The row's hint word, read one tile ahead of its use so that the load's
+  // latency hides behind a tile of work; `seen` is the value in use now.
+  uint32_t seen = 0u, pending = 0u;
+  // The ticket of the last finished segment is checked a tile later, so that
+  // the warp never waits for the atomic's return (lane 0 only).
+  bool tk_pending = false;
+  uint32_t tk_before = 0u, tk_mine = 0u;
+  int64_t tk_row = 0;
   int slot = 0;
+  // Rare list (dense path): entries pending an exact pass, and the bound of the
+  // tile that listed the last of them.
+  unsigned char* rbase = wbase + kStages * C::kTileBytes;
+  int rcnt = 0;
+  Prune pr_last{INFINITY, -INFINITY, false};
 
   while (true) {
     // The current tile has landed (this lane's copies, then everyone's).
@@ -529,18 +744,19 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
     if (rc.T > 0.0f) {
       if (seg_first) {
         lane_candidate<DT, VEC>(stage, t0, t_hi, rc, bs, bi);
-        seen = 0ull;
+        seen = 0u;
       } else {
         seen = pending;
       }
-      pending = __ldcg(&rc.ws->key);
-      // One warp reduction gives both the key to publish (fire-and-forget)
-      // and the bound L for this tile.
-      unsigned long long wk = (bi != INT32_MAX && bs > -INFINITY) ? pack_key(bs, bi) : 0ull;
-      wk = warp_max_u64(wk);
-      if (lane == 0 && wk > seen) atomicMax(&rc.ws->key, wk);
-      const float L = score_of_key(wk > seen ? wk : seen);
+      pending = __ldcg(&rc.ws->hint);
+      // The best exact score this warp knows; publish it (fire-and-forget) if
+      // it beats what the row had, and prune against the larger of the two.
+      const float wbest = warp_max_f32(bs);
+      const uint32_t wb = wbest > -INFINITY ? ordered_bits(wbest) : 0u;
+      if (lane == 0 && wb > seen) atomicMax(&rc.ws->hint, wb);
+      const float L = fmaxf(wbest, score_of_hint(seen));
       const Prune pr = make_prune(L, rc.T);
+#if GSAMPLE_COMPACT
       uint32_t thr2 = 0;
       if constexpr (!C::kF32Bits) thr2 = packed_threshold<DT>(pr.thr_x);
 
@@ -575,6 +791,10 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
       }
       __syncwarp();
       phase_c<DT, VEC>(stage, list, cnt, (uint32_t)t0 * C::kGPU, rc, pr, bs, bi);
+#else
+      pr_last = pr;
+      dense_tile<DT, VEC>(stage, (uint32_t)t0 * C::kGPU, rc, pr, rbase, rcnt, bs, bi);
+#endif
     } else {
 #pragma unroll
       for (int k = 0; k < kVPT; ++k) {
@@ -584,26 +804,31 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
 
+    if (lane == 0 && tk_pending) {
+      finish_row_if_last(p, tk_row, tk_before, tk_mine, NU);
+      tk_pending = false;
+    }
     if (cur.t_hi == cur.seg_hi) {
-      // This warp's part of row b is done: merge it, then count it in the
-      // row's ticket; the warp that completes the count writes the answer.
+      // This warp's part of row b is done: merge its best, then add its units
+      // to the row's ticket; the warp that brings the count to NU writes the
+      // answer and clears the row's slot (checked one tile later).
+      if (rcnt > 0) {
+        flush_rare<DT, VEC>(rbase, rcnt, rc, pr_last, bs, bi);
+        rcnt = 0;
+      }
       warp_argmax(bs, bi);
       if (lane == 0) {
         if (bi != INT32_MAX && bs > -INFINITY) atomicMax(&rc.ws->key, pack_key(bs, bi));
         __threadfence();
-        const int64_t expected =
-            owner_warp(cur.b * NU + NU - 1, U, NW) - owner_warp(cur.b * NU, U, NW) + 1;
-        const unsigned t = atomicAdd(&rc.ws->ticket, 1u);
-        if ((int64_t)t == expected - 1) {
-          __threadfence();
-          const unsigned long long key = atomicExch(&rc.ws->key, 0ull);
-          atomicExch(&rc.ws->ticket, 0u);
-          p.out_idx[cur.b] = index_of_key(key);
-        }
+        tk_mine = (uint32_t)(cur.seg_hi - cur.seg_lo);
+        tk_before = atomicAdd(&rc.ws->ticket, tk_mine);
+        tk_row = cur.b;
+        tk_pending = true;
       }
       cur = next_tile<C::kTile>(cur, u_end, NU);
       if (!cur.valid) break;
-      rc = row_context(p, cur.b);
+      rc = row_context_from(p, cur.b, next_params);
+      next_params = load_row_params(p, cur.b + 1);
       bs = -INFINITY;
       bi = INT32_MAX;
       seg_first = true;
@@ -613,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
     }
     slot = slot + 1 == kStages ? 0 : slot + 1;
   }
+  if (lane == 0 && tk_pending) finish_row_if_last(p, tk_row, tk_before, tk_mine, NU);
   cp_async_wait<0>();  // no copy may outlive the warp
 }
 
