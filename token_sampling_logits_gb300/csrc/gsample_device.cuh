@@ -81,12 +81,13 @@ __device__ __forceinline__ PhiloxRow philox_row(uint32_t row, uint32_t off0, uin
   return r;
 }
 
-// Four blocks of a row (groups g[0..3]), interleaved round by round.
-__device__ __forceinline__ void philox_row_x4(const uint32_t (&g)[4], const PhiloxRow& pr,
-                                              uint4 (&out)[4]) {
-  uint4 c[4];
+// N blocks of a row (groups g[0..N-1]), interleaved round by round.
+template <int N>
+__device__ __forceinline__ void philox_row_xn(const uint32_t (&g)[N], const PhiloxRow& pr,
+                                              uint4 (&out)[N]) {
+  uint4 c[N];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < N; ++j) {
     const unsigned long long a = (unsigned long long)kPhiloxM0 * g[j];
     const uint32_t z = (uint32_t)(a >> 32) ^ pr.u2;
     const unsigned long long b = (unsigned long long)kPhiloxM1 * z;
@@ -96,7 +97,7 @@ __device__ __forceinline__ void philox_row_x4(const uint32_t (&g)[4], const Phil
 #pragma unroll
   for (int round = 2; round < 10; ++round) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < N; ++j) {
       const unsigned long long p0 = (unsigned long long)kPhiloxM0 * c[j].x;
       const unsigned long long p1 = (unsigned long long)kPhiloxM1 * c[j].z;
       c[j] = make_uint4((uint32_t)(p1 >> 32) ^ c[j].y ^ k0, (uint32_t)p1,
@@ -106,7 +107,12 @@ __device__ __forceinline__ void philox_row_x4(const uint32_t (&g)[4], const Phil
     k1 += kPhiloxW1;
   }
 #pragma unroll
-  for (int j = 0; j < 4; ++j) out[j] = c[j];
+  for (int j = 0; j < N; ++j) out[j] = c[j];
+}
+
+__device__ __forceinline__ void philox_row_x4(const uint32_t (&g)[4], const PhiloxRow& pr,
+                                              uint4 (&out)[4]) {
+  philox_row_xn<4>(g, pr, out);
 }
 
 __device__ __forceinline__ uint4 philox_row_1(uint32_t g, const PhiloxRow& pr) {

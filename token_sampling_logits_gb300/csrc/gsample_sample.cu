@@ -29,8 +29,8 @@
 // independent blocks per lane at a time, and a cheap bound on g from the
 // largest word of the block rejects almost every group before the two exact
 // logarithms. The few survivors wait in a per-warp list and are scored 32 at a
-// time, one per lane. (A compaction variant, GSAMPLE_COMPACT, lists the groups
-// that pass the logit threshold and runs Philox only on those.)
+// time, one per lane. Where only a small share of a tile's groups reaches the
+// logit threshold, those groups are compacted first and only they get Philox.
 #include <cstdint>
 #include <type_traits>
 
@@ -49,9 +49,6 @@ namespace {
 #endif
 #ifndef GSAMPLE_MIN_CTAS_PER_SM
 #define GSAMPLE_MIN_CTAS_PER_SM 2
-#endif
-#ifndef GSAMPLE_COMPACT
-#define GSAMPLE_COMPACT 0
 #endif
 constexpr int kVPT = GSAMPLE_VPT;        // units per lane per tile
 constexpr int kStages = GSAMPLE_STAGES;  // tiles per warp ring
@@ -326,45 +323,6 @@ __device__ __forceinline__ void score_group(uint32_t gid, float x0, float x1, fl
   *bi_io = bi;
 }
 
-// The four logits of tile-local group q (q = unit-in-tile * kGPU + h).
-template <int DT, bool VEC>
-__device__ __forceinline__ void group_values(uint32_t stage, uint32_t q, float x[4]) {
-  using C = Cfg<DT, VEC>;
-  if constexpr (C::kF32Bits) {
-    const uint4 d = lds128(stage + q * 16u);
-    x[0] = __uint_as_float(d.x);
-    x[1] = __uint_as_float(d.y);
-    x[2] = __uint_as_float(d.z);
-    x[3] = __uint_as_float(d.w);
-  } else {
-    const uint2 d = lds64(stage + q * 8u);  // kGPU == 2: unit q/2, half q%2
-    x[0] = half_to_f32<DT>(d.x & 0xFFFFu);
-    x[1] = half_to_f32<DT>(d.x >> 16);
-    x[2] = half_to_f32<DT>(d.y & 0xFFFFu);
-    x[3] = half_to_f32<DT>(d.y >> 16);
-  }
-}
-
-// A list entry: tile-local group index q and the group's largest logit. 16-bit
-// inputs pack both in one word (q low, the 16-bit maximum high); binary32 needs
-// two words.
-template <int DT, bool VEC>
-struct ListEntry {
-  using T = typename std::conditional<Cfg<DT, VEC>::kF32Bits, uint2, uint32_t>::type;
-};
-
-template <int DT, bool VEC>
-__device__ __forceinline__ void decode_entry(const typename ListEntry<DT, VEC>::T& e, uint32_t& q,
-                                             float& xm) {
-  if constexpr (Cfg<DT, VEC>::kF32Bits) {
-    q = e.x;
-    xm = __uint_as_float(e.y);
-  } else {
-    q = e & 0xFFFFu;
-    xm = half_to_f32<DT>(e >> 16);
-  }
-}
-
 // Can the group still reach L, given its largest logit and largest Philox word
 // (v = 1 - u only shrinks as the word grows, so one test covers all four)?
 __device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const Prune& pr,
@@ -373,87 +331,19 @@ __device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const 
   return may_reach(xm, max(max(w.x, w.y), max(w.z, w.w)), rt);
 }
 
-// Phase C: the tile's surviving groups, four per lane at a time so that a lane
-// keeps four independent Philox chains in flight. The few groups that pass the
-// group-level test are not scored on the spot (one lane would keep the other
-// 31 idle through two logarithms): their list entries are compacted into the
-// already-consumed front of the list and scored afterwards, one per lane.
-template <int DT, bool VEC>
-__device__ __forceinline__ void phase_c(uint32_t stage, typename ListEntry<DT, VEC>::T* list,
-                                        int cnt, uint32_t g0, const RowCtx& rc, const Prune& pr,
-                                        float& bs, int32_t& bi) {
-  using Entry = typename ListEntry<DT, VEC>::T;
-  const int lane = threadIdx.x & 31;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  const ReachTest rt = make_reach(pr, rc.rT);
-  int rcnt = 0;  // deferred entries, stored in list[0, rcnt) (always <= entries read so far)
-  const int full = cnt & ~127;
-  for (int base = 0; base < full; base += 128) {
-    Entry e[4];
-    uint32_t g[4];
-    float xm[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t q;
-      e[j] = list[base + lane + 32 * j];
-      decode_entry<DT, VEC>(e[j], q, xm[j]);
-      g[j] = g0 + q;
-    }
-    uint4 w[4];
-    philox_row_x4(g, rc.ph, w);
-    uint32_t need = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) need |= group_may_reach(xm[j], w[j], pr, rt) ? (1u << j) : 0u;
-    if (__any_sync(0xFFFFFFFFu, need != 0u)) {
-      __syncwarp();  // every lane has read this round's entries
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool keep = (need >> j) & 1u;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-        if (keep) list[rcnt + __popc(m & lt_mask)] = e[j];
-        rcnt += __popc(m);
-      }
-    }
-  }
-  for (int base = full; base < cnt; base += 32) {
-    const int pa = base + lane;
-    const bool valid = pa < cnt;
-    Entry e = valid ? list[pa] : Entry{};
-    uint32_t q;
-    float xm;
-    decode_entry<DT, VEC>(e, q, xm);
-    const uint4 w = philox_row_1(g0 + q, rc.ph);
-    const bool keep = valid && group_may_reach(xm, w, pr, rt);
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-    if (m) {
-      __syncwarp();
-      if (keep) list[rcnt + __popc(m & lt_mask)] = e;
-      rcnt += __popc(m);
-    }
-  }
-  if (rcnt == 0) return;
-  __syncwarp();
-  for (int p = lane; p < rcnt; p += 32) {
-    uint32_t q;
-    float xm;
-    decode_entry<DT, VEC>(list[p], q, xm);
-    const uint32_t g = g0 + q;
-    const uint4 w = philox_row_1(g, rc.ph);
-    float x[4];
-    group_values<DT, VEC>(stage, q, x);
-    score_group(g, x[0], x[1], x[2], x[3], w, pr, rt, rc.T, &bs, &bi);
-  }
-}
-
 // Groups that passed the cheap test wait in a per-warp list, across tiles,
 // until 32 of them (or the end of the warp's part of the row) make one exact
 // pass with every lane busy. An entry holds the row-local group index and the
 // group's four logits as stored in the tile (so the ring stage may be reused).
 constexpr int kRareCap = 32;
 constexpr uint32_t kRareRawOff = kRareCap * 4;  // byte offset of the logits array
-static_assert(kRareRawOff + kRareCap * 16 <= Cfg<0, true>::kListBytes &&
-                  kRareRawOff + kRareCap * 8 <= Cfg<1, true>::kListBytes,
-              "the rare list must fit in a warp's list area");
+// A warp's list area holds the rare list, then the compacted list of a tile
+// (one 16-bit tile-local group index per surviving group).
+constexpr int kRareBytes = (int)kRareRawOff + kRareCap * 16;
+static_assert(kRareBytes + Cfg<0, true>::kCap * 2 <= Cfg<0, true>::kListBytes &&
+                  kRareBytes + Cfg<1, true>::kCap * 2 <= Cfg<1, true>::kListBytes &&
+                  kRareBytes + Cfg<1, false>::kCap * 2 <= Cfg<1, false>::kListBytes,
+              "the rare list and a tile's compacted list must fit in a warp's list area");
 
 template <int DT, bool VEC>
 using RareRaw = typename std::conditional<Cfg<DT, VEC>::kF32Bits, uint4, uint2>::type;
@@ -496,19 +386,117 @@ __device__ __forceinline__ uint32_t lane_group(int i, int lane) {
   return (uint32_t)(((i / C::kGPU) * 32 + lane) * C::kGPU + i % C::kGPU);
 }
 
-// Dense pass over a sampled tile, written as straight-line code so that the
-// shared-memory reads, the four-way Philox batches and the tests of different
-// batches can overlap. One vote skips the whole tile when no logit in it
-// reaches the logit threshold; otherwise every group of the tile gets its
-// Philox block and the word-level test, and the few survivors go to the rare
-// list.
+// Groups whose word test passed join the rare list: one round per set bit of
+// the lane's `need` mask. Bit j stands for tile-local group q[j], or, with N ==
+// 0, for the lane's j-th group of the tile.
+template <int DT, bool VEC, int N>
+__device__ __forceinline__ void append_rare(uint32_t need, const uint32_t* q, uint32_t stage,
+                                            uint32_t g0, const RowCtx& rc, const Prune& pr,
+                                            unsigned char* rbase, int& rcnt, float& bs,
+                                            int32_t& bi) {
+  using C = Cfg<DT, VEC>;
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  while (__any_sync(0xFFFFFFFFu, need != 0u)) {
+    const bool has = need != 0u;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, has);
+    const int n = __popc(m);
+    if (rcnt + n > kRareCap) {
+      flush_rare<DT, VEC>(rbase, rcnt, rc, pr, bs, bi);
+      rcnt = 0;
+    }
+    if (has) {
+      const int jj = __ffs(need) - 1;
+      need &= need - 1u;
+      uint32_t qq;
+      if constexpr (N == 0) {
+        qq = lane_group<DT, VEC>(jj, lane);
+      } else {
+        qq = q[0];
+#pragma unroll
+        for (int j = 1; j < N; ++j)
+          if (jj == j) qq = q[j];
+      }
+      const int s = rcnt + __popc(m & lt_mask);
+      reinterpret_cast<uint32_t*>(rbase)[s] = g0 + qq;
+      auto* raw = reinterpret_cast<RareRaw<DT, VEC>*>(rbase + kRareRawOff);
+      if constexpr (C::kF32Bits) {
+        raw[s] = lds128(stage + qq * 16u);
+      } else {
+        raw[s] = lds64(stage + qq * 8u);
+      }
+    }
+    rcnt += n;
+  }
+}
+
+// The largest logit of tile-local group q, read back from the stage.
 template <int DT, bool VEC>
-__device__ __forceinline__ void dense_tile(uint32_t stage, uint32_t g0, const RowCtx& rc,
-                                            const Prune& pr, unsigned char* rbase, int& rcnt,
-                                            float& bs, int32_t& bi) {
+__device__ __forceinline__ float group_max_at(uint32_t stage, uint32_t q) {
+  if constexpr (Cfg<DT, VEC>::kF32Bits) {
+    const uint4 d = lds128(stage + q * 16u);
+    return fmaxf(fmaxf(__uint_as_float(d.x), __uint_as_float(d.y)),
+                 fmaxf(__uint_as_float(d.z), __uint_as_float(d.w)));
+  } else {
+    const uint2 d = lds64(stage + q * 8u);
+    const uint32_t m = hmax2_bits<DT>(d.x, d.y);
+    return fmaxf(half_to_f32<DT>(m & 0xFFFFu), half_to_f32<DT>(m >> 16));
+  }
+}
+
+// One batch of the compacted list: entries [base, base + 32 * N) below cnt,
+// N Philox blocks per lane side by side.
+template <int DT, bool VEC, int N>
+__device__ __forceinline__ void compact_batch(uint32_t stage, const unsigned short* clist, int base,
+                                              int cnt, uint32_t g0, const RowCtx& rc,
+                                              const Prune& pr, const ReachTest& rt,
+                                              unsigned char* rbase, int& rcnt, float& bs,
+                                              int32_t& bi) {
+  const int lane = threadIdx.x & 31;
+  uint32_t q[N], g[N];
+  float xm[N];
+  bool valid[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const int idx = base + lane + 32 * j;
+    valid[j] = idx < cnt;
+    q[j] = valid[j] ? (uint32_t)clist[idx] : 0u;
+    xm[j] = group_max_at<DT, VEC>(stage, q[j]);
+    g[j] = g0 + q[j];
+  }
+  uint4 w[N];
+  philox_row_xn<N>(g, rc.ph, w);
+  uint32_t need = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    need |= (valid[j] && group_may_reach(xm[j], w[j], pr, rt)) ? (1u << j) : 0u;
+  append_rare<DT, VEC, N>(need, q, stage, g0, rc, pr, rbase, rcnt, bs, bi);
+}
+
+#ifndef GSAMPLE_DENSE_NUM
+#define GSAMPLE_DENSE_NUM 1  // dense when more than NUM/DEN of the tile's groups survive
+#endif
+#ifndef GSAMPLE_DENSE_DEN
+#define GSAMPLE_DENSE_DEN 8
+#endif
+
+// A sampled tile. Each lane first takes the largest logit of each of its
+// groups; when none in the warp reaches the logit threshold the tile is
+// skipped. The share of groups that do is estimated from 128 of them (each
+// lane's first four). A large share (above GSAMPLE_DENSE_NUM/DEN): every group
+// gets its Philox block, four per lane side by side, as straight-line code.
+// Otherwise the survivors' tile-local indices are compacted into a list and
+// only they get Philox, 128 per warp batch (a short last batch runs one or two
+// blocks per lane). Either way the word test follows, and the rare groups that
+// pass it join the rare list.
+template <int DT, bool VEC>
+__device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const RowCtx& rc,
+                                             const Prune& pr, unsigned char* rbase,
+                                             unsigned short* clist, int& rcnt, float& bs,
+                                             int32_t& bi) {
   using C = Cfg<DT, VEC>;
   constexpr int NG = kVPT * C::kGPU;  // groups per lane in a tile
-  static_assert(NG % 4 == 0, "groups per lane must fill four-way Philox batches");
+  static_assert(NG % 4 == 0 && NG <= 32, "groups per lane must fill four-way Philox batches");
   const int lane = threadIdx.x & 31;
   float xm[NG];
 #pragma unroll
@@ -527,44 +515,53 @@ __device__ __forceinline__ void dense_tile(uint32_t stage, uint32_t g0, const Ro
 #pragma unroll
   for (int i = 1; i < NG; ++i) tm = fmaxf(tm, xm[i]);
   if (!__any_sync(0xFFFFFFFFu, tm >= pr.thr_x)) return;  // nothing here can win
-
   const ReachTest rt = make_reach(pr, rc.rT);
-  uint32_t need = 0;
+
+  // The share of surviving groups, estimated from each lane's first four.
+  int c4 = 0;
 #pragma unroll
-  for (int b = 0; b < NG; b += 4) {
-    uint32_t g[4];
+  for (int i = 0; i < 4; ++i) c4 += xm[i] >= pr.thr_x ? 1 : 0;
+  const int sample = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)c4);
+  if (sample * GSAMPLE_DENSE_DEN > 128 * GSAMPLE_DENSE_NUM) {
+    uint32_t need = 0;
+    const uint32_t gl = g0 + lane_group<DT, VEC>(0, lane);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) g[j] = g0 + lane_group<DT, VEC>(b + j, lane);
-    uint4 w[4];
-    philox_row_x4(g, rc.ph, w);
+    for (int b = 0; b < NG; b += 4) {
+      uint32_t g[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      need |= group_may_reach(xm[b + j], w[j], pr, rt) ? (1u << (b + j)) : 0u;
+      for (int j = 0; j < 4; ++j)
+        g[j] = gl + (uint32_t)(((b + j) / C::kGPU) * 32 * C::kGPU + (b + j) % C::kGPU);
+      uint4 w[4];
+      philox_row_x4(g, rc.ph, w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        need |= group_may_reach(xm[b + j], w[j], pr, rt) ? (1u << (b + j)) : 0u;
+    }
+    append_rare<DT, VEC, 0>(need, nullptr, stage, g0, rc, pr, rbase, rcnt, bs, bi);
+    return;
   }
 
   const unsigned lt_mask = (1u << lane) - 1u;
-  while (__any_sync(0xFFFFFFFFu, need != 0u)) {
-    const bool has = need != 0u;
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, has);
-    const int n = __popc(m);
-    if (rcnt + n > kRareCap) {
-      flush_rare<DT, VEC>(rbase, rcnt, rc, pr, bs, bi);
-      rcnt = 0;
-    }
-    if (has) {
-      const uint32_t q = lane_group<DT, VEC>(__ffs(need) - 1, lane);
-      need &= need - 1u;
-      const int s = rcnt + __popc(m & lt_mask);
-      reinterpret_cast<uint32_t*>(rbase)[s] = g0 + q;
-      auto* raw = reinterpret_cast<RareRaw<DT, VEC>*>(rbase + kRareRawOff);
-      if constexpr (C::kF32Bits) {
-        raw[s] = lds128(stage + q * 16u);
-      } else {
-        raw[s] = lds64(stage + q * 8u);
-      }
-    }
-    rcnt += n;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NG; ++i) {
+    const bool keep = xm[i] >= pr.thr_x;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+    if (keep) clist[cnt + __popc(m & lt_mask)] = (unsigned short)lane_group<DT, VEC>(i, lane);
+    cnt += __popc(m);
   }
+  __syncwarp();
+  for (int base = 0; base < cnt; base += 128) {
+    const int r = cnt - base;
+    if (r > 64) {
+      compact_batch<DT, VEC, 4>(stage, clist, base, cnt, g0, rc, pr, rt, rbase, rcnt, bs, bi);
+    } else if (r > 32) {
+      compact_batch<DT, VEC, 2>(stage, clist, base, cnt, g0, rc, pr, rt, rbase, rcnt, bs, bi);
+    } else {
+      compact_batch<DT, VEC, 1>(stage, clist, base, cnt, g0, rc, pr, rt, rbase, rcnt, bs, bi);
+    }
+  }
+  __syncwarp();  // the list is read before the next tile rewrites it
 }
 
 // Phase A: this lane's largest logit of the tile, scored exactly.
@@ -688,8 +685,6 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
   const int lane = threadIdx.x & 31;
   unsigned char* wbase = smem + (size_t)warp * C::kWarpBytes;
   const uint32_t ring = smem_addr(wbase);
-  using Entry = typename ListEntry<DT, VEC>::T;
-  Entry* list = reinterpret_cast<Entry*>(wbase + kStages * C::kTileBytes);
   const uint64_t pol = evict_first_policy();
 
   const int64_t U = p.total_units, NU = p.units_per_row, NW = p.warps;
@@ -756,45 +751,9 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
       if (lane == 0 && wb > seen) atomicMax(&rc.ws->hint, wb);
       const float L = fmaxf(wbest, score_of_hint(seen));
       const Prune pr = make_prune(L, rc.T);
-#if GSAMPLE_COMPACT
-      uint32_t thr2 = 0;
-      if constexpr (!C::kF32Bits) thr2 = packed_threshold<DT>(pr.thr_x);
-
-      // Phase B: list the groups of the tile that may still win.
-      int cnt = 0;
-      const unsigned lt_mask = (1u << lane) - 1u;
-#pragma unroll
-      for (int k = 0; k < kVPT; ++k) {
-        const uint4 r = lds128(stage + (uint32_t)(k * 32 + lane) * 16u);
-#pragma unroll
-        for (int h = 0; h < C::kGPU; ++h) {
-          const uint32_t q = (uint32_t)((k * 32 + lane) * C::kGPU + h);
-          if constexpr (C::kF32Bits) {
-            const float gm = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
-                                   fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
-            const bool keep = gm >= pr.thr_x;
-            const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
-            if (keep) list[cnt + __popc(mask & lt_mask)] = make_uint2(q, __float_as_uint(gm));
-            cnt += __popc(mask);
-          } else {
-            const uint32_t m2 = h == 0 ? hmax2_bits<DT>(r.x, r.y) : hmax2_bits<DT>(r.z, r.w);
-            const bool keep = hge2_any<DT>(m2, thr2);
-            const unsigned mask = __ballot_sync(0xFFFFFFFFu, keep);
-            if (keep) {
-              // the larger half of the pair, as a 16-bit value, next to q
-              const uint32_t mm = hmax2_bits<DT>(m2, __funnelshift_l(m2, m2, 16));
-              list[cnt + __popc(mask & lt_mask)] = q | (mm << 16);
-            }
-            cnt += __popc(mask);
-          }
-        }
-      }
-      __syncwarp();
-      phase_c<DT, VEC>(stage, list, cnt, (uint32_t)t0 * C::kGPU, rc, pr, bs, bi);
-#else
       pr_last = pr;
-      dense_tile<DT, VEC>(stage, (uint32_t)t0 * C::kGPU, rc, pr, rbase, rcnt, bs, bi);
-#endif
+      sampled_tile<DT, VEC>(stage, (uint32_t)t0 * C::kGPU, rc, pr, rbase,
+                            reinterpret_cast<unsigned short*>(rbase + kRareBytes), rcnt, bs, bi);
     } else {
 #pragma unroll
       for (int k = 0; k < kVPT; ++k) {
