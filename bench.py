@@ -111,6 +111,31 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Integer-pipe roofline of Philox4x32-10. One block takes ten rounds of two
+# 32x32->64-bit products; the kernels fold the first two rounds' row-uniform
+# products into per-row constants, leaving 18 per block. A 64-bit product is
+# two 32-bit integer multiply-adds, and an SM retires 64 of those per clock
+# (the CUDA programming guide's throughput table for compute capability 9/10).
+PHILOX_PRODUCTS_PER_BLOCK = 18
+IMAD_PER_CLOCK_PER_SM = 64
+
+
+def alu_peak(sms: int):
+    """Philox blocks per second that the integer multiply pipe allows at the
+    maximum SM clock (MEASURED_PEAKS.json's, else the part's 2070 MHz)."""
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except Exception:
+        pass
+    per_sm_per_clock = IMAD_PER_CLOCK_PER_SM / 2.0 / PHILOX_PRODUCTS_PER_BLOCK
+    return sms * mhz * 1e6 * per_sm_per_clock, (
+        "derived: %d SMs x %.0f MHz x %d integer multiply-adds per clock per SM / 2 per "
+        "64-bit product / %d products per block" % (sms, mhz, IMAD_PER_CLOCK_PER_SM,
+                                                   PHILOX_PRODUCTS_PER_BLOCK))
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons around the timed
     region."""
@@ -463,6 +488,19 @@ def run_ours(args, dist: Dist):
     alg_bytes = batch.B * (batch.V * 2 + PER_ROW_PARAM_BYTES)
     achieved = alg_bytes / (us_step * 1e-6) / 1e9
     peak, peak_kind = hbm_peak()
+    # The method draws one Philox word per element: B * ceil(V / 4) blocks.
+    alg_blocks = batch.B * ((batch.V + 3) // 4)
+    blocks_per_s = alg_blocks / (us_step * 1e-6)
+    apeak, apeak_kind = alu_peak(props.multi_processor_count)
+    hbm_view = {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind + " (copy bandwidth)",
+                "floor_us": round(alg_bytes / (peak * 1e9) * 1e6, 2)}
+    alu_view = {"achieved": round(blocks_per_s, 1), "peak": round(apeak, 1),
+                "unit": "Philox4x32-10 blocks/s", "frac": round(blocks_per_s / apeak, 4),
+                "peak_kind": apeak_kind, "floor_us": round(alg_blocks / apeak * 1e6, 2)}
+    # The binding roof is the one with the longer floor time.
+    bound = "alu" if alu_view["floor_us"] > hbm_view["floor_us"] else "hbm"
+    main = alu_view if bound == "alu" else hbm_view
 
     e2e = None
     if not args.quick:
@@ -496,12 +534,13 @@ def run_ours(args, dist: Dist):
         "us_per_step": round(us_step, 3),
         "GBps": round(achieved, 1),
         "frac_of_8TBps": round(achieved / 8000.0, 4),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind + " (copy bandwidth)",
+        "roofline": {"bound": bound, "achieved": main["achieved"], "peak": main["peak"],
+                     "unit": main["unit"], "frac": main["frac"], "peak_kind": main["peak_kind"],
                      "traffic": ncu_traffic("sample_kernel_bf16_throughput.md", batch.B),
                      "kernel": "gsample::sample_kernel<bf16, 128-bit>",
-                     "algorithmic_bytes_per_launch": alg_bytes},
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_blocks_per_launch": alg_blocks,
+                     "hbm": hbm_view, "alu": alu_view},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,

@@ -1,0 +1,98 @@
+"""Host-side logic of bench.py without a GPU: the max-over-ranks reduction and
+the whole-job aggregate across a world of two gloo ranks, the kernel-source
+hash that invalidates stored ncu traffic, and the derived integer-pipe peak."""
+import importlib.util
+import os
+import socket
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(WORLD_SIZE=str(world), RANK=str(rank), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    b = _bench()
+    d = b.Dist(world)
+    # rank r "ran" 100 * (r + 1) rows in 1.5 + r seconds
+    t = d.max(1.5 + rank)
+    rows = d.max(100.0 * (rank + 1))  # the largest share, to check the reduction
+    d.barrier()
+    d.close()
+    q.put((rank, t, rows))
+
+
+def test_two_rank_gloo_reduction_and_aggregate():
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert [g[1] for g in got] == [2.5, 2.5]  # every rank sees the slowest rank's time
+    assert [g[2] for g in got] == [200.0, 200.0]
+    b = _bench()
+    assert b.aggregate([100.0, 200.0], [1.5, 2.5]) == pytest.approx(120.0)
+
+
+def test_kernel_source_hash_tracks_sources(tmp_path, monkeypatch):
+    b = _bench()
+    h = b.kernel_source_hash()
+    assert len(h) == 16 and h == b.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1000\n"
+                               "captured_rows: 10\n" % h)
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    # ROOT now points at a folder without the sources: the hash no longer matches
+    with pytest.raises(OSError):
+        b.kernel_source_hash()
+
+
+def test_stored_traffic_is_scaled_and_nulled_on_source_change(tmp_path, monkeypatch):
+    b = _bench()
+    h = b.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1000\n"
+                               "captured_rows: 10\n" % h)
+    (prof / "q.md").write_text("kernel_source_hash: 0000000000000000\n"
+                               "dram_bytes_per_launch: 1000\ncaptured_rows: 10\n")
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: h)
+    assert b.ncu_traffic("p.md", 30) == pytest.approx(3000.0)
+    assert b.ncu_traffic("q.md", 30) is None
+    assert b.ncu_traffic("missing.md", 30) is None
+
+
+def test_integer_pipe_peak_from_unit_counts():
+    b = _bench()
+    peak, kind = b.alu_peak(152)
+    # 152 SMs x 2070 MHz x 64 / 2 / 18
+    import json
+
+    try:
+        mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        mhz = 2070.0
+    assert peak == pytest.approx(152 * mhz * 1e6 * 64 / 2 / 18, rel=1e-9)
+    assert kind.startswith("derived")
