@@ -11,14 +11,19 @@
 // so sweep 1 only needs the row max (top) or the softmax-weighted mean of the
 // logits (entropy, accumulated online as max / sum e^(x-max) / sum e^(x-max) x).
 //
-// Layout: one thread-block cluster of `cluster` CTAs per row. Each CTA streams
-// its slice of the row from HBM once, keeping it in shared memory (RESIDENT),
-// reduces its partial statistics, and the cluster exchanges them through
-// distributed shared memory after a hardware cluster barrier. Sweep 2 then
-// scores the slice from shared memory. If a slice is too large for shared
-// memory the same kernel re-reads it from global memory in sweep 2
-// (!RESIDENT). Candidates merge through the same packed-key workspace as the
-// plain sampler; no CTA ever spins on another.
+// Layout: one thread-block cluster of `cluster` CTAs (512 threads each) per
+// row. Each CTA requests its whole slice of the row at once with cp.async into
+// shared memory (RESIDENT), reduces its partial statistics, and the cluster
+// exchanges them through distributed shared memory after a hardware cluster
+// barrier. Sweep 2 scores the slice from shared memory: the logit threshold
+// from the inverse curve, then Philox four groups per thread at a time, then a
+// word bound (g <= -log(1 - u)) on a fast upper bound of the curve, and the
+// exact score only for the rare groups that pass. Each CTA's best (score,
+// index) key goes to rank 0 over distributed shared memory, which writes the
+// row's answer: the row needs no global atomics and leaves the workspace
+// untouched. If a slice is too large for shared memory the same kernel
+// re-reads it from global memory in sweep 2 (!RESIDENT). The only waits are
+// hardware cluster and CTA barriers.
 #include <cooperative_groups.h>
 
 #include <cstdint>
@@ -85,6 +90,29 @@ __device__ __forceinline__ uint4 load_unit(const char* row, int32_t u, int32_t V
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+constexpr int kHlgThreads = 512;
+constexpr int kHlgWarps = kHlgThreads / 32;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 // Online softmax moments of finite logits: M = max x, S = sum e^(x-M),
 // W = sum e^(x-M) x. Empty: M = -inf, S = W = 0.
 struct Moments {
@@ -123,6 +151,20 @@ __device__ __forceinline__ float tone(const Curve& c, float z) {
   return c.m * z;
 }
 
+// An upper bound of tone(z) for pruning only: the fast logarithm of 1 + t
+// errs by a few 1e-7 relative, far inside the 1e-4 relative slack added.
+__device__ __forceinline__ float tone_upper(const Curve& c, float z) {
+  float y;
+  if (z < -c.w) {
+    y = -c.m * c.w - c.m * c.bt * __logf(1.0f + (-z - c.w) * c.rbt);
+  } else if (z > c.w) {
+    y = c.m * c.w + c.m * c.bh * __logf(1.0f + (z - c.w) * c.rbh);
+  } else {
+    y = c.m * z;
+  }
+  return y + 1e-4f * (1.0f + fabsf(y));
+}
+
 // z below which the curve stays under Y (the inverse curve), or -inf.
 __device__ __forceinline__ float tone_inverse(const Curve& c, float Y) {
   const float mw = c.m * c.w;
@@ -143,12 +185,28 @@ __device__ __forceinline__ float hlg_score(const Curve& c, const RowState& rs, f
   return y * rT + gumbel_of_word(word);
 }
 
+// Block-wide (score, index) argmax; every thread gets the result. `red` holds
+// kHlgWarps packed keys.
+__device__ __forceinline__ unsigned long long block_best(float s, int32_t i,
+                                                         unsigned long long* red) {
+  warp_argmax(s, i);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = (i != INT32_MAX && s > -INFINITY) ? pack_key(s, i) : 0ull;
+  __syncthreads();
+  unsigned long long k = lane < kHlgWarps ? red[lane] : 0ull;
+  k = warp_max_u64(k);
+  __syncthreads();  // red may be reused
+  return k;
+}
+
 template <int DT, bool VEC, bool RESIDENT>
-__global__ void __launch_bounds__(kThreads) hlg_kernel(const HlgParams p) {
+__global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   using C = HCfg<DT, VEC>;
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ Moments s_warp[kWarps];
-  __shared__ Moments s_part;  // this CTA's partial, read by the whole cluster
+  __shared__ Moments s_warp[kHlgWarps];
+  __shared__ Moments s_part;            // this CTA's partial, read by the whole cluster
+  __shared__ unsigned long long s_red[kHlgWarps];
+  __shared__ unsigned long long s_best;  // this CTA's best key, read by rank 0
   __shared__ int s_pinf;
   __shared__ RowState s_row;
 
@@ -160,50 +218,77 @@ __global__ void __launch_bounds__(kThreads) hlg_kernel(const HlgParams p) {
   const int32_t u_lo = rank * p.units_per_cta;
   const int32_t u_hi = min(NU, u_lo + p.units_per_cta);
   const char* row = p.logits + b * p.ld_bytes;
-  uint4* slice = reinterpret_cast<uint4*>(smem);
+  const uint32_t slice = (uint32_t)__cvta_generic_to_shared(smem);
   const uint64_t pol = evict_first_policy();
-  WsRow* ws = p.ws + b;
 
   const float T = __ldg(p.temperature + b);
   const bool sampled = T > 0.0f;
   const bool entropy = p.pivot_mode == 1;
   if (threadIdx.x == 0) s_pinf = 0;
-  __syncthreads();
 
-  // Sweep 1: stream the slice once; statistics (sampled) or argmax (greedy).
-  Moments mo{-INFINITY, 0.0f, 0.0f};
-  float bs = -INFINITY;
-  int32_t bi = INT32_MAX;
-  bool pinf = false;
+  // Sweep 1: stream the slice once. On the resident path every unit of the
+  // thread's share is requested at once (cp.async into the slice), so the whole
+  // slice is in flight together; the thread then reads back its own units.
+  if constexpr (RESIDENT) {
+    for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
+      const uint32_t dst = slice + (uint32_t)(u - u_lo) * 16u;
+      if (VEC && (u + 1) * C::kEPU <= p.V)
+        cp_async16(dst, row + (size_t)u * 16, pol);
+      else
+        sts128(dst, load_unit<DT, VEC>(row, u, p.V, pol));
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  }
+  auto unit_at = [&](int32_t u) -> uint4 {
+    if constexpr (RESIDENT)
+      return lds128(slice + (uint32_t)(u - u_lo) * 16u);
+    else
+      return load_unit<DT, VEC>(row, u, p.V, pol);
+  };
+  // The thread's largest logit (lowest index on ties): the greedy answer, and
+  // the first exact candidate of a sampled row. For the pivot, the largest
+  // finite logit; +inf is flagged.
   float cand_x = -INFINITY;
   int32_t cand_i = INT32_MAX;
-  for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kThreads) {
-    const uint4 r = load_unit<DT, VEC>(row, u, p.V, pol);
-    if constexpr (RESIDENT) slice[u - u_lo] = r;
+  float fmax_x = -INFINITY;
+  bool pinf = false;
+  for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
+    const uint4 r = unit_at(u);
 #pragma unroll
     for (int e = 0; e < C::kEPU; ++e) {
       const float x = elt<DT, VEC>(r, e);
-      const int32_t i = u * C::kEPU + e;
-      if (x > cand_x) {  // greedy answer, and the first candidate of a sampled row
+      if (x > cand_x) {
         cand_x = x;
-        cand_i = i;
+        cand_i = u * C::kEPU + e;
       }
-      if (sampled) {
-        if (x == INFINITY) pinf = true;
-        if (entropy) {
-          if (x > -INFINITY && x < INFINITY) push(mo, x);
-        } else if (x < INFINITY) {
-          mo.M = fmaxf(mo.M, x);
-        }
-      }
+      if (x == INFINITY) pinf = true;
+      else fmax_x = fmaxf(fmax_x, x);
     }
   }
 
+  float bs = -INFINITY;
+  int32_t bi = INT32_MAX;
   if (!sampled) {
     bs = cand_x;
     bi = cand_x > -INFINITY ? cand_i : INT32_MAX;
   } else {
-    // Cluster-wide pivot statistics.
+    // Pivot statistics of the slice. Entropy: a second pass over the slice
+    // (shared memory) sums e^(x - M) and e^(x - M) x against the thread's max.
+    Moments mo{fmax_x, 0.0f, 0.0f};
+    if (entropy && fmax_x > -INFINITY) {
+      for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
+        const uint4 r = unit_at(u);
+#pragma unroll
+        for (int e = 0; e < C::kEPU; ++e) {
+          const float x = elt<DT, VEC>(r, e);
+          if (x > -INFINITY && x < INFINITY) {
+            const float ex = __expf(x - fmax_x);
+            mo.S += ex;
+            mo.W = fmaf(ex, x, mo.W);
+          }
+        }
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       Moments other;
@@ -215,37 +300,44 @@ __global__ void __launch_bounds__(kThreads) hlg_kernel(const HlgParams p) {
     if (__any_sync(0xFFFFFFFFu, pinf) && lane == 0) atomicOr(&s_pinf, 1);
     if (lane == 0) s_warp[warp] = mo;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      Moments acc = s_warp[0];
-      for (int k = 1; k < kWarps; ++k)
-        acc = entropy ? merge(acc, s_warp[k]) : Moments{fmaxf(acc.M, s_warp[k].M), 0.0f, 0.0f};
-      if (s_pinf) acc.M = INFINITY;  // flag travels with the partial
-      s_part = acc;
+    if (warp == 0) {
+      Moments acc = lane < kHlgWarps ? s_warp[lane] : Moments{-INFINITY, 0.0f, 0.0f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        Moments other;
+        other.M = __shfl_xor_sync(0xFFFFFFFFu, acc.M, o);
+        other.S = __shfl_xor_sync(0xFFFFFFFFu, acc.S, o);
+        other.W = __shfl_xor_sync(0xFFFFFFFFu, acc.W, o);
+        acc = entropy ? merge(acc, other) : Moments{fmaxf(acc.M, other.M), 0.0f, 0.0f};
+      }
+      if (lane == 0) {
+        if (s_pinf) acc.M = INFINITY;  // the flag travels with the partial
+        s_part = acc;
+      }
     }
     cluster.sync();
     if (warp == 0) {
-      Moments acc{-INFINITY, 0.0f, 0.0f};
-      bool any_pinf = false;
-      // Every CTA merges the same partials in the same (rank) order, so all
-      // CTAs of the row get bit-identical pivot statistics.
-      for (int k = 0; k < p.cluster; ++k) {
-        const Moments* rp = cluster.map_shared_rank(&s_part, k);
-        Moments o = *rp;
-        if (o.M == INFINITY) {
-          any_pinf = true;
-          continue;
-        }
-        acc = entropy ? merge(acc, o) : Moments{fmaxf(acc.M, o.M), 0.0f, 0.0f};
+      // Lane k reads CTA k's partial; the same butterfly on every CTA gives
+      // all CTAs of the row bit-identical pivot statistics.
+      Moments o{-INFINITY, 0.0f, 0.0f};
+      if (lane < p.cluster) o = *cluster.map_shared_rank(&s_part, lane);
+      const bool any_pinf = __any_sync(0xFFFFFFFFu, o.M == INFINITY);
+      if (o.M == INFINITY) o = Moments{-INFINITY, 0.0f, 0.0f};
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        Moments other;
+        other.M = __shfl_xor_sync(0xFFFFFFFFu, o.M, off);
+        other.S = __shfl_xor_sync(0xFFFFFFFFu, o.S, off);
+        other.W = __shfl_xor_sync(0xFFFFFFFFu, o.W, off);
+        o = entropy ? merge(o, other) : Moments{fmaxf(o.M, other.M), 0.0f, 0.0f};
       }
       if (lane == 0) {
         RowState rs;
         rs.pinf = any_pinf;
-        rs.shift = entropy ? -(acc.W / acc.S) : (p.pivot_offset - acc.M);
+        rs.shift = entropy ? -(o.W / o.S) : (p.pivot_offset - o.M);
         s_row = rs;
       }
     }
-    // Done reading other CTAs' shared memory; the matching wait is at the end.
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     __syncthreads();
     const RowState rs = s_row;
 
@@ -255,29 +347,20 @@ __global__ void __launch_bounds__(kThreads) hlg_kernel(const HlgParams p) {
     const uint32_t k0 = (uint32_t)sd, k1 = (uint32_t)(sd >> 32);
     const uint32_t o0 = (uint32_t)of, o1 = (uint32_t)(of >> 32);
     const uint32_t row_id = (uint32_t)b;
+    const PhiloxRow ph = philox_row(row_id, o0, o1, k0, k1);
 
-    // First candidate: this thread's largest logit, scored exactly.
+    // First candidate: this thread's largest logit, scored exactly; the CTA's
+    // best of them is the bound L that sweep 2 prunes against.
     if (cand_i != INT32_MAX && cand_x > -INFINITY && (!rs.pinf || cand_x == INFINITY)) {
-      const uint4 blk = philox4x32_10(make_uint4((uint32_t)cand_i >> 2, row_id, o0, o1), k0, k1);
+      const uint4 blk = philox_row_1((uint32_t)cand_i >> 2, ph);
       take_better(hlg_score(cv, rs, cand_x, word_of(blk, cand_i & 3), rT), cand_i, bs, bi);
     }
-    float L;
-    {
-      float s = bs;
-      int32_t i = bi;
-      warp_argmax(s, i);
-      unsigned long long old = 0ull;
-      if (lane == 0) {
-        if (i != INT32_MAX && s > -INFINITY)
-          old = atomicMax(&ws->key, pack_key(s, i));
-        else
-          old = __ldcg(&ws->key);
-      }
-      old = __shfl_sync(0xFFFFFFFFu, old, 0);
-      L = fmaxf(s, score_of_key(old));
-    }
+    const float L = score_of_key(block_best(bs, bi, s_red));
+
     // Exact pruning in logit space: x < x_thr implies tone(x + shift)/T + max g < L.
     float x_thr = -INFINITY;
+    bool word_test = false;
+    float wa = 0.0f, wc = 0.0f;
     if (rs.pinf || L == INFINITY) {
       x_thr = INFINITY;
     } else if (L > -INFINITY && T >= 1e-20f && T <= 1e20f) {
@@ -285,49 +368,77 @@ __global__ void __launch_bounds__(kThreads) hlg_kernel(const HlgParams p) {
       const float z_thr = tone_inverse(cv, (L - kGumbelMax - margin) * T);
       x_thr = z_thr - rs.shift - 1e-3f * (1.0f + fabsf(z_thr)) - 1e-3f * (1.0f + fabsf(rs.shift));
       if (!(x_thr == x_thr)) x_thr = -INFINITY;  // NaN guard: no pruning
+      // Word bound: g <= -log(1 - u), so a group whose curve value is at most
+      // y can reach L only if 1 - u(max word) <= 2^((y / T - lm) log2 e).
+      constexpr float kLog2e = 1.4426950408889634f;
+      const float lm = L - margin - 0.01f;
+      word_test = true;
+      wa = rT * kLog2e;
+      wc = -lm * kLog2e;
     }
 
-    // Sweep 2 over the slice, four-element Philox groups.
-    for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kThreads) {
-      uint4 r;
-      if constexpr (RESIDENT)
-        r = slice[u - u_lo];
-      else
-        r = load_unit<DT, VEC>(row, u, p.V, pol);
+    // Sweep 2 over the slice: four 4-element Philox groups per thread at a
+    // time (four units of binary32, two of 16-bit), one Philox block each.
+    constexpr int kUPB = 4 / C::kGPU;  // units per batch
+    const int32_t n_iter = (u_hi - u_lo + kHlgThreads - 1) / kHlgThreads;
+    for (int32_t it = 0; it < n_iter; it += kUPB) {
+      uint4 r[kUPB];
+      float xm[4];
+      uint32_t g[4];
+      bool ok[4];
 #pragma unroll
-      for (int h = 0; h < C::kGPU; ++h) {
-        float gm = elt<DT, VEC>(r, 4 * h);
+      for (int j = 0; j < kUPB; ++j) {
+        const int32_t u = u_lo + threadIdx.x + (it + j) * kHlgThreads;
+        const bool valid = u < u_hi;
+        r[j] = valid ? unit_at(u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int e = 1; e < 4; ++e) gm = fmaxf(gm, elt<DT, VEC>(r, 4 * h + e));
-        if (!(gm >= x_thr)) continue;
-        const uint32_t gid = (uint32_t)(u * C::kGPU + h);
-        const uint4 blk = philox4x32_10(make_uint4(gid, row_id, o0, o1), k0, k1);
+        for (int h = 0; h < C::kGPU; ++h) {
+          float gm = elt<DT, VEC>(r[j], 4 * h);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float x = elt<DT, VEC>(r, 4 * h + t);
-          if (!(x >= x_thr) || x == -INFINITY) continue;
-          take_better(hlg_score(cv, rs, x, word_of(blk, t), rT), (int32_t)(4 * gid + t), bs, bi);
+          for (int e = 1; e < 4; ++e) gm = fmaxf(gm, elt<DT, VEC>(r[j], 4 * h + e));
+          const int jj = j * C::kGPU + h;
+          xm[jj] = gm;
+          ok[jj] = valid && gm >= x_thr;
+          g[jj] = (uint32_t)(u * C::kGPU + h);
+        }
+      }
+      if (!__any_sync(0xFFFFFFFFu, ok[0] || ok[1] || ok[2] || ok[3])) continue;
+      uint4 w[4];
+      philox_row_x4(g, ph, w);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        bool need = ok[jj];
+        if (need && word_test) {
+          const uint32_t wm = max(max(w[jj].x, w[jj].y), max(w[jj].z, w[jj].w));
+          need = may_reach(tone_upper(cv, xm[jj] + rs.shift), wm, ReachTest{wa, wc});
+        }
+        if (need) {  // rare: the exact scores of the group's elements
+          const uint4 rj = r[jj / C::kGPU];
+          const int h = jj % C::kGPU;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float x = elt<DT, VEC>(rj, 4 * h + t);
+            if (!(x >= x_thr) || x == -INFINITY) continue;
+            take_better(hlg_score(cv, rs, x, word_of(w[jj], t), rT), (int32_t)(4 * g[jj] + t),
+                        bs, bi);
+          }
         }
       }
     }
   }
 
-  // Merge into the row's key; the last CTA of the row writes the answer.
-  warp_argmax(bs, bi);
-  if (lane == 0 && bi != INT32_MAX && bs > -INFINITY) atomicMax(&ws->key, pack_key(bs, bi));
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned t = atomicAdd(&ws->ticket, 1u);
-    if ((int)t == p.cluster - 1) {
-      __threadfence();
-      const unsigned long long key = atomicExch(&ws->key, 0ull);
-      atomicExch(&ws->ticket, 0u);
-      p.out_idx[b] = index_of_key(key);
-    }
+  // The row's answer: each CTA's best key, merged by rank 0 over distributed
+  // shared memory. The second cluster barrier keeps every CTA's shared memory
+  // alive until rank 0 has read it.
+  const unsigned long long best = block_best(bs, bi, s_red);
+  if (threadIdx.x == 0) s_best = best;
+  cluster.sync();
+  if (rank == 0 && warp == 0) {
+    unsigned long long k = lane < p.cluster ? *cluster.map_shared_rank(&s_best, lane) : 0ull;
+    k = warp_max_u64(k);
+    if (lane == 0) p.out_idx[b] = index_of_key(k);
   }
-  // Shared memory must outlive the cluster's remote reads of s_part.
-  if (sampled) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  cluster.sync();
 }
 
 template <int DT, bool VEC, bool RES>
@@ -373,7 +484,7 @@ int hlg_max_cluster(int dtype, bool vec, size_t smem_bytes) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(16);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kHlgThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -395,7 +506,7 @@ cudaError_t launch_hlg(const HlgParams& p, int dtype, bool vec, cudaStream_t str
   void* fn = select_hlg(dtype, vec, resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.cluster));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kHlgThreads);
   cfg.dynamicSmemBytes = resident ? need : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
