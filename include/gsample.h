@@ -128,6 +128,22 @@ gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype
                                          const gsample_hlg_params* hlg, int64_t* out_idx,
                                          void* workspace, gsample_stream_t stream);
 
+/* gsample_hlg_gumbel_argmax with one curve per row ("HLG sampling", section
+ * "Where it lands in the code": each batched row owns its sampler, so the
+ * curve parameters batch per request). hlg_rows: DEVICE array of B
+ * gsample_hlg_params (24 bytes each, 4-byte aligned), read by the kernel.
+ * Device data cannot be checked at the call, so a row whose parameters fail
+ * the checks of gsample_hlg_gumbel_argmax (finite m > 0, w >= 0 (may be
+ * +inf), finite beta_t > 0 and beta_h > 0, finite pivot_offset, a known
+ * pivot_mode) gets out_idx[b] = -1; rows with temperature <= 0 or NaN are
+ * greedy whatever their curve. Everything else as gsample_hlg_gumbel_argmax. */
+gsample_status gsample_hlg_gumbel_argmax_rows(const void* logits, gsample_dtype dtype, int64_t B,
+                                              int64_t V, int64_t ld, const float* temperature,
+                                              const uint64_t* seed, const uint64_t* offset,
+                                              const gsample_hlg_params* hlg_rows,
+                                              int64_t* out_idx, void* workspace,
+                                              gsample_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gsample_status_string(gsample_status status);
 

@@ -109,3 +109,17 @@ def test_no_device_is_an_error_not_a_fallback():
     # valid-looking arguments reach the device query, which must fail loudly
     assert _gumbel() == gs.ERR_CUDA
     assert gs.lib().gsample_argmax(FAKE, gs.BF16, 2, 64, 64, FAKE, FAKE, None) == gs.ERR_CUDA
+
+
+def test_per_row_hlg_entry_validation():
+    L = gs.lib()
+
+    def call(B=4, rows=FAKE, out=FAKE, logits=FAKE):
+        return L.gsample_hlg_gumbel_argmax_rows(logits, gs.F32, B, 100, 100, FAKE, FAKE, FAKE,
+                                                rows, out, FAKE, None)
+
+    assert call(B=0, rows=None) == gs.OK              # empty batch: nothing to do
+    assert call(rows=None) == gs.ERR_INVALID_ARG       # B > 0 needs the per-row array
+    assert call(rows=FAKE + 2) == gs.ERR_INVALID_ARG   # 24-byte records of 4-byte fields
+    assert call(out=None) == gs.ERR_INVALID_ARG
+    assert call(logits=None) == gs.ERR_INVALID_ARG

@@ -115,3 +115,59 @@ def test_hlg_greedy_rows_untouched():
     got = gpu_hlg(b, params())
     ref, _ = oracle.argmax(b.logits)
     assert np.array_equal(got, ref)
+
+
+def _rows_oracle(b, curves):
+    ref, gap = oracle.hlg_gumbel_argmax(
+        b.logits, b.temperature, b.seed, b.offset, m=[c.m for c in curves], w=[c.w for c in curves],
+        beta_t=[c.beta_t for c in curves], beta_h=[c.beta_h for c in curves],
+        c=[c.pivot_offset for c in curves], pivot_mode=[c.pivot_mode for c in curves],
+        dtype=b.dtype)
+    return ref, gap
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_hlg_per_row_curves(dtype):
+    """One curve per row ("HLG sampling", "Where it lands in the code": batched
+    rows carry per-request parameters): each row matches the oracle with its
+    own curve, and equals a launch-wide call made with that curve."""
+    rng = np.random.default_rng([41, dtype])
+    B, V = 6, 20000
+    x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+    x[rng.random((B, V)) < 0.005] = -np.inf
+    T = np.array([1.0, 0.7, 0.0, 1.3, 1.0, 0.9], np.float32)
+    b = W.Batch("hlg_rows", W.encode(x, dtype), dtype, T, W.splitmix64(8, B),
+                np.full(B, 3, np.uint64))
+    curves = [params(gs.PIVOT_TOP), params(gs.PIVOT_ENTROPY, m=0.8, w=1.0),
+              params(gs.PIVOT_TOP, m=5.0), params(gs.PIVOT_TOP, m=2.0, w=0.5, beta_t=0.5,
+                                                  beta_h=3.0, pivot_offset=3.0),
+              params(gs.PIVOT_ENTROPY, m=1.0, w=float("inf")), params(gs.PIVOT_TOP, pivot_offset=-2.0)]
+    xd = to_device(b.logits, b.dtype)
+    got = gs.hlg_gumbel_argmax_rows(xd, torch.from_numpy(T).cuda(),
+                                    gs.seeds_as_tensor(b.seed, "cuda"),
+                                    gs.seeds_as_tensor(b.offset, "cuda"), curves)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    ref, gap = _rows_oracle(b, curves)
+    Tally().add(got, ref, gap, greedy_mask=~(T > 0), where="per-row curves")
+    for r in range(B):
+        single = gpu_hlg(b, curves[r], logits_dev=xd)
+        assert single[r] == got[r], (r, single[r], got[r])
+
+
+def test_hlg_per_row_invalid_curve_gives_minus_one():
+    rng = np.random.default_rng(5)
+    B, V = 4, 3000
+    x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    T = np.array([1.0, 1.0, 0.0, 1.0], np.float32)
+    b = W.Batch("hlg_bad", x, W.F32, T, W.splitmix64(2, B), np.zeros(B, np.uint64))
+    curves = [params(), params(m=-1.0), params(pivot_mode=7), params(beta_h=float("nan"))]
+    got = gs.hlg_gumbel_argmax_rows(to_device(x, W.F32), torch.from_numpy(T).cuda(),
+                                    gs.seeds_as_tensor(b.seed, "cuda"),
+                                    gs.seeds_as_tensor(b.offset, "cuda"), curves)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    assert got[1] == -1 and got[3] == -1          # sampled rows with a failing curve
+    assert got[2] == int(np.argmax(x[2]))         # a greedy row ignores its curve
+    ref, gap = _rows_oracle(b, [curves[0]] * B)
+    Tally().add(got[:1], ref[:1], gap[:1], where="valid row beside invalid ones")

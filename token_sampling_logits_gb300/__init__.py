@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
                                              _vp]),
             "gsample_hlg_gumbel_argmax": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                                  _vp, _vp, _vp]),
+            "gsample_hlg_gumbel_argmax_rows": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                      _vp, _vp, _vp, _vp]),
             "gsample_status_string": (ctypes.c_char_p, [_int]),
             "gsample_debug_philox": (_int, [_u64, _u32, _u64, _i64, _i64, _vp, _vp]),
             "gsample_debug_gumbel": (_int, [_vp, _i64, _vp, _vp, _vp]),
@@ -242,6 +244,40 @@ def hlg_gumbel_argmax(logits, temperature, seed, offset, hlg: HlgParams, out=Non
                                          S.data_ptr(), O.data_ptr(), ctypes.byref(hp),
                                          out.data_ptr(), ws.data_ptr(), _stream_ptr(dev))
     _check(st, "gsample_hlg_gumbel_argmax")
+    return out
+
+
+def hlg_rows_tensor(params, device):
+    """Per-row curves as the device array gsample_hlg_gumbel_argmax_rows reads:
+    B records of 24 bytes (five float32 fields, then the int32 pivot mode)."""
+    import numpy as np
+
+    torch = _torch()
+    rec = np.dtype([("m", "<f4"), ("w", "<f4"), ("beta_t", "<f4"), ("beta_h", "<f4"),
+                    ("pivot_offset", "<f4"), ("pivot_mode", "<i4")])
+    a = np.zeros(len(params), dtype=rec)
+    for i, h in enumerate(params):
+        a[i] = (h.m, h.w, h.beta_t, h.beta_h, h.pivot_offset, h.pivot_mode)
+    return torch.from_numpy(a.view(np.uint8).copy()).to(device)
+
+
+def hlg_gumbel_argmax_rows(logits, temperature, seed, offset, params, out=None, workspace=None):
+    """HLG + Gumbel-max with one curve per row. `params`: a list of B HlgParams,
+    or a uint8 device tensor from hlg_rows_tensor."""
+    torch = _torch()
+    dt, B, V, ld, out, ws = _prepare(logits, out, workspace)
+    dev = logits.device
+    T = _row_tensor(temperature, B, torch.float32, dev, "temperature")
+    S = _row_tensor(seed, B, torch.int64, dev, "seed")
+    O = _row_tensor(offset, B, torch.int64, dev, "offset")
+    if not torch.is_tensor(params):
+        params = hlg_rows_tensor(params, dev)
+    if params.device != dev or params.dtype != torch.uint8 or params.numel() != 24 * B:
+        raise ValueError("per-row HLG parameters: a uint8 tensor of 24*B bytes on the logits' device")
+    st = lib().gsample_hlg_gumbel_argmax_rows(logits.data_ptr(), dt, B, V, ld, T.data_ptr(),
+                                              S.data_ptr(), O.data_ptr(), params.data_ptr(),
+                                              out.data_ptr(), ws.data_ptr(), _stream_ptr(dev))
+    _check(st, "gsample_hlg_gumbel_argmax_rows")
     return out
 
 

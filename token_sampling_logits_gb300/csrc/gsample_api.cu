@@ -164,12 +164,17 @@ gsample_status check_hlg(const gsample_hlg_params* h) {
 
 gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
                        const float* temperature, const uint64_t* seed, const uint64_t* offset,
-                       const gsample_hlg_params* hlg, int64_t* out_idx, void* workspace,
-                       int32_t ctas_override, cudaStream_t stream) {
+                       const gsample_hlg_params* hlg, const gsample_hlg_params* hlg_rows,
+                       int64_t* out_idx, void* workspace, int32_t ctas_override,
+                       cudaStream_t stream) {
   gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
   if (st != GSAMPLE_OK) return st;
-  if (check_hlg(hlg) != GSAMPLE_OK || !temperature || !seed || !offset)
+  if (hlg_rows) {
+    if ((uintptr_t)hlg_rows % 4) return GSAMPLE_ERR_INVALID_ARG;
+  } else if (check_hlg(hlg) != GSAMPLE_OK) {
     return GSAMPLE_ERR_INVALID_ARG;
+  }
+  if (!temperature || !seed || !offset) return GSAMPLE_ERR_INVALID_ARG;
   if (B == 0) return GSAMPLE_OK;
   const DeviceInfo* d = nullptr;
   st = device_info(&d);
@@ -206,12 +211,18 @@ gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64
   p.offset = offset;
   p.out_idx = out_idx;
   p.ws = static_cast<WsRow*>(workspace);
-  p.m = hlg->m;
-  p.w = hlg->w;
-  p.beta_t = hlg->beta_t;
-  p.beta_h = hlg->beta_h;
-  p.pivot_offset = hlg->pivot_offset;
-  p.pivot_mode = hlg->pivot_mode;
+  if (hlg_rows) {
+    static_assert(sizeof(gsample_hlg_params) == sizeof(gsample::HlgRowParams),
+                  "the public and internal per-row layouts must agree");
+    p.rows = reinterpret_cast<const gsample::HlgRowParams*>(hlg_rows);
+  } else {
+    p.m = hlg->m;
+    p.w = hlg->w;
+    p.beta_t = hlg->beta_t;
+    p.beta_h = hlg->beta_h;
+    p.pivot_offset = hlg->pivot_offset;
+    p.pivot_mode = hlg->pivot_mode;
+  }
   const cudaError_t err = gsample::launch_hlg(p, (int)dtype, vec, stream);
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -263,8 +274,20 @@ gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype
                                          const uint64_t* seed, const uint64_t* offset,
                                          const gsample_hlg_params* hlg, int64_t* out_idx,
                                          void* workspace, gsample_stream_t stream) {
-  return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, out_idx, workspace, 0,
-                 (cudaStream_t)stream);
+  return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, nullptr, out_idx,
+                 workspace, 0, (cudaStream_t)stream);
+}
+
+gsample_status gsample_hlg_gumbel_argmax_rows(const void* logits, gsample_dtype dtype, int64_t B,
+                                              int64_t V, int64_t ld, const float* temperature,
+                                              const uint64_t* seed, const uint64_t* offset,
+                                              const gsample_hlg_params* hlg_rows,
+                                              int64_t* out_idx, void* workspace,
+                                              gsample_stream_t stream) {
+  if (B == 0) return check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (!hlg_rows) return GSAMPLE_ERR_INVALID_ARG;
+  return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, nullptr, hlg_rows, out_idx,
+                 workspace, 0, (cudaStream_t)stream);
 }
 
 const char* gsample_status_string(gsample_status status) {
@@ -314,8 +337,8 @@ gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, 
                                        void* workspace, int32_t ctas, gsample_stream_t stream) {
   if (ctas < 0) return GSAMPLE_ERR_INVALID_ARG;
   if (hlg)
-    return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, out_idx, workspace,
-                   ctas, (cudaStream_t)stream);
+    return run_hlg(logits, dtype, B, V, ld, temperature, seed, offset, hlg, nullptr, out_idx,
+                   workspace, ctas, (cudaStream_t)stream);
   if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
   return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, ctas,
                     (cudaStream_t)stream);

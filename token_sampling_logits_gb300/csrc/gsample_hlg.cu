@@ -165,6 +165,15 @@ __device__ __forceinline__ float tone_upper(const Curve& c, float z) {
   return y + 1e-4f * (1.0f + fabsf(y));
 }
 
+// The checks the host applies to a launch-wide curve, for per-row curves that
+// only the device sees: finite m > 0, w >= 0 (+inf allowed), finite
+// beta_t, beta_h > 0, finite pivot offset, pivot mode 0 (top) or 1 (entropy).
+__device__ __forceinline__ bool curve_ok(const HlgRowParams& h) {
+  return isfinite(h.m) && h.m > 0.0f && h.w >= 0.0f && isfinite(h.beta_t) && h.beta_t > 0.0f &&
+         isfinite(h.beta_h) && h.beta_h > 0.0f && isfinite(h.pivot_offset) &&
+         (h.pivot_mode == 0 || h.pivot_mode == 1);
+}
+
 // z below which the curve stays under Y (the inverse curve), or -inf.
 __device__ __forceinline__ float tone_inverse(const Curve& c, float Y) {
   const float mw = c.m * c.w;
@@ -222,8 +231,19 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   const uint64_t pol = evict_first_policy();
 
   const float T = __ldg(p.temperature + b);
+  // The row's curve: the launch's, or its own from the per-row array.
+  HlgRowParams hp{p.m, p.w, p.beta_t, p.beta_h, p.pivot_offset, p.pivot_mode};
+  if (p.rows) {
+    const HlgRowParams* r = p.rows + b;
+    hp = HlgRowParams{__ldg(&r->m), __ldg(&r->w), __ldg(&r->beta_t), __ldg(&r->beta_h),
+                      __ldg(&r->pivot_offset), __ldg(&r->pivot_mode)};
+  }
   const bool sampled = T > 0.0f;
-  const bool entropy = p.pivot_mode == 1;
+  if (sampled && !curve_ok(hp)) {  // a per-row curve that fails the checks: no answer
+    if (rank == 0 && threadIdx.x == 0) p.out_idx[b] = -1;
+    return;  // every CTA of the cluster reads the same row, so all leave here
+  }
+  const bool entropy = hp.pivot_mode == 1;
   if (threadIdx.x == 0) s_pinf = 0;
 
   // Sweep 1: stream the slice once. On the resident path every unit of the
@@ -334,14 +354,14 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
       if (lane == 0) {
         RowState rs;
         rs.pinf = any_pinf;
-        rs.shift = entropy ? -(o.W / o.S) : (p.pivot_offset - o.M);
+        rs.shift = entropy ? -(o.W / o.S) : (hp.pivot_offset - o.M);
         s_row = rs;
       }
     }
     __syncthreads();
     const RowState rs = s_row;
 
-    const Curve cv{p.m, p.w, p.beta_t, p.beta_h, 1.0f / p.beta_t, 1.0f / p.beta_h};
+    const Curve cv{hp.m, hp.w, hp.beta_t, hp.beta_h, 1.0f / hp.beta_t, 1.0f / hp.beta_h};
     const float rT = 1.0f / T;
     const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
     const uint32_t k0 = (uint32_t)sd, k1 = (uint32_t)(sd >> 32);

@@ -29,6 +29,13 @@ struct SampleParams {
   WsRow* ws;
 };
 
+// One row's curve; the same layout as the public gsample_hlg_params.
+struct HlgRowParams {
+  float m, w, beta_t, beta_h, pivot_offset;
+  int32_t pivot_mode;
+};
+static_assert(sizeof(HlgRowParams) == 24, "per-row HLG parameters are six 4-byte fields");
+
 // HLG launch: one thread-block cluster of `cluster` CTAs per row.
 struct HlgParams {
   const char* logits;
@@ -45,6 +52,7 @@ struct HlgParams {
   WsRow* ws;
   float m, w, beta_t, beta_h, pivot_offset;
   int32_t pivot_mode;
+  const HlgRowParams* rows;  // per-row curves (device), or nullptr: the fields above
 };
 
 // Elements per unit for a dtype code (0 f32, 1 bf16, 2 f16) and load path.
