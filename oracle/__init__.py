@@ -81,6 +81,10 @@ def _load():
                                              _dbl, _dbl, _dbl, _int, _vp, _vp]),
             "oracle_hlg_gumbel_argmax": (None, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+            "oracle_categorical_row": (_i64, [_vp, _int, _i64, _flt, _u64, _u32, _u64, _i64,
+                                              _vp, _vp]),
+            "oracle_categorical": (None, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                                          _vp, _vp]),
             "oracle_philox_blocks": (None, [_u32, _u32, _vp, _i64, _vp]),
             "oracle_stream_words": (None, [_u64, _u32, _u64, _i64, _i64, _vp]),
             "oracle_gumbel_of_words": (None, [_vp, _i64, _vp]),
@@ -211,6 +215,37 @@ def hlg_sample_row(row: np.ndarray, temperature: float, seed: int, row_id: int, 
                                     m, w, beta_t, beta_h, c, pivot_mode, ctypes.byref(gap),
                                     ctypes.byref(best))
     return int(idx), gap.value, best.value
+
+
+def categorical_row(row: np.ndarray, temperature: float, seed: int, row_id: int, offset: int,
+                    probe: int = -1, dtype: int | None = None):
+    """Inverse-CDF sample of softmax(row / T) with element 0's uniform.
+    -> (idx, margin, probe_dist): margin and probe_dist relative to the row's sum."""
+    lib = _load()
+    row = np.ascontiguousarray(row)
+    dt = _dtype_code(row, dtype)
+    margin = ctypes.c_double()
+    pd = ctypes.c_double()
+    idx = lib.oracle_categorical_row(_ptr(row), dt, row.size, temperature, seed, row_id, offset,
+                                     probe, ctypes.byref(pd), ctypes.byref(margin))
+    return int(idx), margin.value, pd.value
+
+
+def categorical(logits: np.ndarray, temperature, seed, offset, probe=None,
+                dtype: int | None = None):
+    """Categorical (inverse-CDF) sample per row. probe: optional int64[B] of
+    indices to locate against the exact CDF. -> (idx, margin, probe_dist)."""
+    lib = _load()
+    x, B, V, ld = _logits_2d(logits)
+    dt = _dtype_code(x, dtype)
+    T, S, O = _row_arrays(B, temperature, seed, offset)
+    pr = None if probe is None else np.ascontiguousarray(np.asarray(probe, dtype=np.int64))
+    idx = np.zeros(B, dtype=np.int64)
+    margin = np.zeros(B, dtype=np.float64)
+    pd = np.zeros(B, dtype=np.float64)
+    lib.oracle_categorical(_ptr(x), dt, B, V, ld, _ptr(T), _ptr(S), _ptr(O), _ptr(pr), _ptr(idx),
+                           _ptr(margin), _ptr(pd))
+    return idx, margin, pd
 
 
 def _row_arrays(B, temperature, seed, offset):

@@ -407,6 +407,86 @@ void oracle_hlg_gumbel_argmax(const void* logits, int dtype, int64_t B, int64_t 
 }
 
 /* ----------------------------------------------------------------------------
+ * [CATEG] The categorical path that the issue benchmarks Gumbel-max against
+ * ("Softmax-free GPU sampling", Background: a normalisation pass over the
+ * vocabulary, then a categorical draw; "Performance validation": baseline
+ * categorical path vs Gumbel-max). Plain inverse-CDF sampling of
+ * softmax(x / T) with one uniform per row:
+ *   M = the largest finite logit, p_i = exp((x_i - M) / T) (0 for -inf/NaN),
+ *   S = sum_i p_i, t = u * S, and the answer is the smallest i whose running
+ *   sum C_i = p_0 + ... + p_i exceeds t (i.e. t lies in [C_{i-1}, C_i)).
+ * The uniform u is the one the Gumbel path gives element 0 (same Philox
+ * stream, same mapping). Temperature <= 0 or NaN is greedy; a row with a +inf
+ * logit returns its lowest +inf index; a row with no candidate returns -1.
+ *   margin (may be NULL): distance from t to the nearer end of the chosen
+ *     interval, relative to S.
+ *   probe >= 0: *probe_dist = distance from t to the interval of element
+ *     `probe`, relative to S (0 when t lies inside it; +inf when p_probe = 0).
+ * ------------------------------------------------------------------------- */
+static double categ_weight(const void* row, int dtype, int64_t i, double M, double T) {
+  double x = oracle_load(row, dtype, i);
+  if (isnan(x) || x == -INFINITY) return 0.0;
+  return exp((x - M) / T);
+}
+
+int64_t oracle_categorical_row(const void* row, int dtype, int64_t V, float temperature,
+                               uint64_t seed, uint32_t row_id, uint64_t offset, int64_t probe,
+                               double* probe_dist, double* margin) {
+  double T = (double)temperature;
+  int64_t ans = -1;
+  if (probe_dist) *probe_dist = INFINITY;
+  if (margin) *margin = INFINITY;
+  if (!(T > 0.0)) {
+    ans = greedy_row(row, dtype, V, NULL);
+    if (probe_dist && probe == ans) *probe_dist = 0.0;
+    return ans;
+  }
+  double M = -INFINITY;
+  for (int64_t i = 0; i < V; ++i) {
+    double x = oracle_load(row, dtype, i);
+    if (x == INFINITY) { /* +inf takes all the mass: its lowest index */
+      if (probe_dist && probe == i) *probe_dist = 0.0;
+      return i;
+    }
+    if (!isnan(x) && x > M) M = x;
+  }
+  if (M == -INFINITY) return -1;
+  double S = 0.0;
+  for (int64_t i = 0; i < V; ++i) S += categ_weight(row, dtype, i, M, T);
+  double u = oracle_uniform(oracle_stream_word(seed, row_id, 0, offset));
+  double t = u * S;
+  double C = 0.0;
+  int64_t last = -1;
+  for (int64_t i = 0; i < V; ++i) {
+    double p = categ_weight(row, dtype, i, M, T);
+    if (p == 0.0) continue;
+    double lo = C;
+    C += p;
+    last = i;
+    if (probe_dist && probe == i) *probe_dist = t < lo ? (lo - t) / S : t >= C ? (t - C) / S : 0.0;
+    if (ans < 0 && t < C) {
+      ans = i;
+      if (margin) *margin = fmin(t - lo, C - t) / S;
+    }
+  }
+  if (ans < 0) ans = last; /* t == S after rounding: the last element with mass */
+  return ans;
+}
+
+void oracle_categorical(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                        const float* temperature, const uint64_t* seed, const uint64_t* offset,
+                        const int64_t* probe, int64_t* out_idx, double* out_margin,
+                        double* out_probe_dist) {
+  for (int64_t b = 0; b < B; ++b) {
+    const char* row = (const char*)logits + b * ld * elt_size(dtype);
+    out_idx[b] = oracle_categorical_row(row, dtype, V, temperature[b], seed[b], (uint32_t)b,
+                                        offset[b], probe ? probe[b] : -1,
+                                        out_probe_dist ? &out_probe_dist[b] : NULL,
+                                        out_margin ? &out_margin[b] : NULL);
+  }
+}
+
+/* ----------------------------------------------------------------------------
  * Batched conveniences for the tests: plain loops over the functions above.
  * ------------------------------------------------------------------------- */
 void oracle_philox_blocks(uint32_t key0, uint32_t key1, const uint32_t* ctrs, int64_t n,
