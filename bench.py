@@ -259,7 +259,8 @@ class Runner:
     """Timed decode steps of one workload through the C ABI, replayed from
     captured CUDA graphs (see the module docstring for the buffer pool)."""
 
-    def __init__(self, batch: W.Batch, hlg=None, min_pool_bytes: int = 0, ring: int = 1000):
+    def __init__(self, batch: W.Batch, hlg=None, min_pool_bytes: int = 0, ring: int = 1000,
+                 categorical: bool = False):
         import ctypes
 
         import torch
@@ -286,6 +287,7 @@ class Runner:
         self.ws = gs.new_workspace(self.B)
         self.dt, _, _, self.ld = gs._logits_args(self.pool[0])
         self.hp = hlg.to_c() if hlg is not None else None
+        self.categorical = categorical
         self.graphs = {}
         self.launches = 0
 
@@ -295,7 +297,12 @@ class Runner:
         B = self.B
         for k in range(n):
             x = self.pool[(k0 + k) % self.P]
-            if self.hp is None:
+            if self.categorical:
+                rc = L.gsample_categorical(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                           self.T.data_ptr(), self.S.data_ptr(),
+                                           self.offs.data_ptr() + 8 * B * k,
+                                           self.out.data_ptr() + 8 * B * k, st)
+            elif self.hp is None:
                 rc = L.gsample_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
                                              self.T.data_ptr(), self.S.data_ptr(),
                                              self.offs.data_ptr() + 8 * B * k,
@@ -438,17 +445,27 @@ def extra_table(dist: Dist, l2: int):
                       pivot_offset=p["c"])
     cases.append(("hlg", W.hlg(), hp))
     cases.append(("mixed_greedy", W.mixed_greedy(), None))
-    for kind, b, h in cases:
-        r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500)
+    def timed(b, h=None, categorical=False):
+        r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500, categorical=categorical)
         steps = r.ring * max(1, (2000 if b.B * b.V < 50_000_000 else 500) // r.ring)
         ms, _ = time_steps(r, steps, 50, dist)
-        us = ms * 1000 / steps
-        nbytes = b.B * (b.V * (4 if b.dtype == W.F32 else 2) + PER_ROW_PARAM_BYTES)
-        rows.append({"workload": kind, "B": b.B, "V": b.V, "dtype": W.DTYPE_NAMES[b.dtype],
-                     "us_per_step": round(us, 3), "rows_per_s": round(b.B / us * 1e6, 1),
-                     "GBps": round(nbytes / us / 1e3, 1),
-                     "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4)})
         del r
+        return ms * 1000 / steps
+
+    for kind, b, h in cases:
+        us = timed(b, h)
+        nbytes = b.B * (b.V * (4 if b.dtype == W.F32 else 2) + PER_ROW_PARAM_BYTES)
+        row = {"workload": kind, "B": b.B, "V": b.V, "dtype": W.DTYPE_NAMES[b.dtype],
+               "us_per_step": round(us, 3), "rows_per_s": round(b.B / us * 1e6, 1),
+               "GBps": round(nbytes / us / 1e3, 1),
+               "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4)}
+        if kind == "sweep":
+            # The issue's comparison: the categorical (softmax + inverse-CDF)
+            # path against Gumbel-max on the same V x B grid.
+            cu = timed(b, categorical=True)
+            row["categorical_us_per_step"] = round(cu, 3)
+            row["categorical_over_gumbel"] = round(cu / us, 3)
+        rows.append(row)
     return rows
 
 

@@ -144,6 +144,23 @@ gsample_status gsample_hlg_gumbel_argmax_rows(const void* logits, gsample_dtype 
                                               int64_t* out_idx, void* workspace,
                                               gsample_stream_t stream);
 
+/* The categorical baseline the issue measures Gumbel-max against ("Softmax-free
+ * GPU sampling", Background and Performance validation): a normalisation of
+ * softmax(logits / T) and one inverse-CDF draw per row,
+ *     out_idx[b] = smallest i with e_0 + ... + e_i > u * S,
+ * e_i = exp((x_i - M) / T) (0 for -inf and NaN), M the largest finite logit,
+ * S = sum e_i, u the uniform of element 0's Philox word of the row's
+ * (seed, offset) stream (the same word gsample_gumbel_argmax gives element 0).
+ * temperature <= 0 or NaN is greedy; a +inf logit takes all the mass (lowest
+ * +inf index); -1 if the row has no candidate. The sums are binary32: the
+ * index is the inverse CDF of a target within about 1e-6 of S of u * S (not
+ * bit-exact against a double-precision CDF). Needs no workspace. Device
+ * pointers, caller stream, asynchronous, host-side validation as above. */
+gsample_status gsample_categorical(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                                   int64_t ld, const float* temperature, const uint64_t* seed,
+                                   const uint64_t* offset, int64_t* out_idx,
+                                   gsample_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gsample_status_string(gsample_status status);
 

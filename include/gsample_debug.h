@@ -38,6 +38,14 @@ gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, 
                                        void* workspace, int32_t ctas,
                                        gsample_stream_t stream);
 
+/* gsample_categorical with an explicit cluster size (CTAs per row, 1..16;
+ * 0 = the library's choice). */
+gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                            int64_t V, int64_t ld, const float* temperature,
+                                            const uint64_t* seed, const uint64_t* offset,
+                                            int64_t* out_idx, int32_t cluster,
+                                            gsample_stream_t stream);
+
 /* Number of CTAs the library would launch for this problem (0 on bad args). */
 int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
                                    const void* logits, int32_t hlg);

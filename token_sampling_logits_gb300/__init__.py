@@ -23,7 +23,8 @@ from . import build as _build
 __all__ = [
     "GSampleError", "HlgParams", "PIVOT_TOP", "PIVOT_ENTROPY", "F32", "BF16", "F16",
     "lib", "library_path", "workspace_bytes", "workspace_init", "new_workspace", "argmax",
-    "gumbel_argmax", "hlg_gumbel_argmax", "status_string",
+    "gumbel_argmax", "hlg_gumbel_argmax", "hlg_gumbel_argmax_rows", "hlg_rows_tensor",
+    "categorical", "status_string",
 ]
 
 F32, BF16, F16 = 0, 1, 2
@@ -93,6 +94,9 @@ def lib() -> ctypes.CDLL:
                                                  _vp, _vp, _vp]),
             "gsample_hlg_gumbel_argmax_rows": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                       _vp, _vp, _vp, _vp]),
+            "gsample_categorical": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+            "gsample_debug_categorical_ex": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                    _vp, _i32, _vp]),
             "gsample_status_string": (ctypes.c_char_p, [_int]),
             "gsample_debug_philox": (_int, [_u64, _u32, _u64, _i64, _i64, _vp, _vp]),
             "gsample_debug_gumbel": (_int, [_vp, _i64, _vp, _vp, _vp]),
@@ -179,7 +183,7 @@ def workspace_init(ws, B: int) -> None:
            "gsample_workspace_init")
 
 
-def _prepare(logits, out, workspace):
+def _prepare(logits, out, workspace, need_ws: bool = True):
     torch = _torch()
     dt, B, V, ld = _logits_args(logits)
     dev = logits.device
@@ -187,6 +191,8 @@ def _prepare(logits, out, workspace):
         out = torch.empty(B, dtype=torch.int64, device=dev)
     elif out.dtype != torch.int64 or out.device != dev or out.shape != (B,) or not out.is_contiguous():
         raise ValueError("out must be a contiguous int64 tensor of shape [B] on the logits' device")
+    if not need_ws:
+        return dt, B, V, ld, out, None
     if workspace is None:
         workspace = new_workspace(B, dev)
     elif workspace.device != dev or workspace.numel() * workspace.element_size() < workspace_bytes(B):
@@ -244,6 +250,27 @@ def hlg_gumbel_argmax(logits, temperature, seed, offset, hlg: HlgParams, out=Non
                                          S.data_ptr(), O.data_ptr(), ctypes.byref(hp),
                                          out.data_ptr(), ws.data_ptr(), _stream_ptr(dev))
     _check(st, "gsample_hlg_gumbel_argmax")
+    return out
+
+
+def categorical(logits, temperature, seed, offset, out=None, cluster: int = 0):
+    """The categorical baseline: softmax(logits / T) drawn by the inverse CDF of
+    element 0's uniform. cluster: CTAs per row (0 = the library's choice)."""
+    torch = _torch()
+    dt, B, V, ld, out, _ = _prepare(logits, out, None, need_ws=False)
+    dev = logits.device
+    T = _row_tensor(temperature, B, torch.float32, dev, "temperature")
+    S = _row_tensor(seed, B, torch.int64, dev, "seed")
+    O = _row_tensor(offset, B, torch.int64, dev, "offset")
+    L = lib()
+    if cluster:
+        st = L.gsample_debug_categorical_ex(logits.data_ptr(), dt, B, V, ld, T.data_ptr(),
+                                            S.data_ptr(), O.data_ptr(), out.data_ptr(), cluster,
+                                            _stream_ptr(dev))
+    else:
+        st = L.gsample_categorical(logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(),
+                                   O.data_ptr(), out.data_ptr(), _stream_ptr(dev))
+    _check(st, "gsample_categorical")
     return out
 
 

@@ -16,6 +16,7 @@ namespace {
 
 using gsample::SampleParams;
 using gsample::HlgParams;
+using gsample::CatParams;
 using gsample::WsRow;
 
 // Largest V: element indices, Philox group indices and the packed key's low
@@ -31,6 +32,7 @@ struct DeviceInfo {
   int sms = 0;
   int sample_slots[6] = {0, 0, 0, 0, 0, 0};  // CTAs per SM, per (dtype, vec)
   int hlg_cluster[6] = {0, 0, 0, 0, 0, 0};   // largest co-schedulable cluster, per (dtype, vec)
+  int cat_cluster[6] = {0, 0, 0, 0, 0, 0};   // the same for the categorical baseline
 };
 
 std::mutex g_mu;
@@ -69,6 +71,12 @@ gsample_status device_info(const DeviceInfo** out) {
             return GSAMPLE_ERR_CUDA;
           }
           d.hlg_cluster[dt * 2 + v] = c;
+          const int cc = gsample::cat_max_cluster(dt, v != 0);
+          if (cc <= 0) {
+            cudaGetLastError();
+            return GSAMPLE_ERR_CUDA;
+          }
+          d.cat_cluster[dt * 2 + v] = cc;
         }
     }
     d.ready = true;
@@ -80,17 +88,18 @@ gsample_status device_info(const DeviceInfo** out) {
 int64_t elt_bytes(gsample_dtype dt) { return dt == GSAMPLE_F32 ? 4 : 2; }
 
 gsample_status check_common(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
-                            int64_t ld, const int64_t* out_idx, const void* ws) {
+                            int64_t ld, const int64_t* out_idx, const void* ws,
+                            bool needs_ws = true) {
   if (dtype != GSAMPLE_F32 && dtype != GSAMPLE_BF16 && dtype != GSAMPLE_F16)
     return GSAMPLE_ERR_INVALID_ARG;
   if (B < 0 || B > kMaxB || V < 1 || V > kMaxV || ld < V) return GSAMPLE_ERR_INVALID_ARG;
   if (B == 0) return GSAMPLE_OK;
-  if (!logits || !out_idx || !ws) return GSAMPLE_ERR_INVALID_ARG;
+  if (!logits || !out_idx || (needs_ws && !ws)) return GSAMPLE_ERR_INVALID_ARG;
   const int64_t e = elt_bytes(dtype);
   if (ld > INT64_MAX / e / B) return GSAMPLE_ERR_INVALID_ARG;
   if ((uintptr_t)logits % (uintptr_t)e) return GSAMPLE_ERR_INVALID_ARG;
   if ((uintptr_t)out_idx % 8) return GSAMPLE_ERR_INVALID_ARG;
-  if ((uintptr_t)ws % 16) return GSAMPLE_ERR_WORKSPACE;
+  if (needs_ws && (uintptr_t)ws % 16) return GSAMPLE_ERR_WORKSPACE;
   return GSAMPLE_OK;
 }
 
@@ -147,6 +156,49 @@ gsample_status run_sample(const void* logits, gsample_dtype dtype, int64_t B, in
   p.ws = static_cast<WsRow*>(workspace);
   const cudaError_t err = gsample::launch_sample(p, (int)dtype, vec, stream);
   if (err != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status run_categorical(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                               int64_t ld, const float* temperature, const uint64_t* seed,
+                               const uint64_t* offset, int64_t* out_idx, int32_t cluster_override,
+                               cudaStream_t stream) {
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, nullptr, false);
+  if (st != GSAMPLE_OK) return st;
+  if (!temperature || !seed || !offset) return GSAMPLE_ERR_INVALID_ARG;
+  if (B == 0) return GSAMPLE_OK;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  const bool vec = vec_path(logits, dtype, ld);
+  const int epu = gsample::units_elems((int)dtype, vec);
+  const int64_t nu = (V + epu - 1) / epu;
+  const int max_cluster = d->cat_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
+  int cluster = cluster_override;
+  if (cluster == 0) {
+    cluster = max_cluster < 1 ? 1 : max_cluster;
+    int64_t cap = (nu + gsample::kThreads - 1) / gsample::kThreads;
+    if (cap < 1) cap = 1;
+    if (cluster > cap) cluster = (int)cap;
+  }
+  if (cluster < 1 || cluster > 16 || cluster > max_cluster) return GSAMPLE_ERR_INVALID_ARG;
+  CatParams p;
+  std::memset(&p, 0, sizeof p);
+  p.logits = static_cast<const char*>(logits);
+  p.ld_bytes = ld * elt_bytes(dtype);
+  p.B = B;
+  p.V = (int32_t)V;
+  p.units_per_row = (int32_t)nu;
+  p.cluster = cluster;
+  p.units_per_cta = (int32_t)((nu + cluster - 1) / cluster);
+  p.temperature = temperature;
+  p.seed = seed;
+  p.offset = offset;
+  p.out_idx = out_idx;
+  if (gsample::launch_categorical(p, (int)dtype, vec, stream) != cudaSuccess) {
     cudaGetLastError();
     return GSAMPLE_ERR_CUDA;
   }
@@ -278,6 +330,14 @@ gsample_status gsample_hlg_gumbel_argmax(const void* logits, gsample_dtype dtype
                  workspace, 0, (cudaStream_t)stream);
 }
 
+gsample_status gsample_categorical(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                                   int64_t ld, const float* temperature, const uint64_t* seed,
+                                   const uint64_t* offset, int64_t* out_idx,
+                                   gsample_stream_t stream) {
+  return run_categorical(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, 0,
+                         (cudaStream_t)stream);
+}
+
 gsample_status gsample_hlg_gumbel_argmax_rows(const void* logits, gsample_dtype dtype, int64_t B,
                                               int64_t V, int64_t ld, const float* temperature,
                                               const uint64_t* seed, const uint64_t* offset,
@@ -342,6 +402,16 @@ gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, 
   if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
   return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, ctas,
                     (cudaStream_t)stream);
+}
+
+gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                            int64_t V, int64_t ld, const float* temperature,
+                                            const uint64_t* seed, const uint64_t* offset,
+                                            int64_t* out_idx, int32_t cluster,
+                                            gsample_stream_t stream) {
+  if (cluster < 0) return GSAMPLE_ERR_INVALID_ARG;
+  return run_categorical(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, cluster,
+                         (cudaStream_t)stream);
 }
 
 int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,

@@ -29,89 +29,17 @@
 #include <cstdint>
 
 #include "gsample_internal.h"
+#include "gsample_slice.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace gsample {
 namespace {
 
-template <int DT, bool VEC>
-struct HCfg {
-  static constexpr int kEPU = VEC ? (DT == 0 ? 4 : 8) : 4;
-  static constexpr int kGPU = kEPU / 4;
-  static constexpr bool kF32Bits = DT == 0 || !VEC;
-};
-
-template <int DT>
-__device__ __forceinline__ float half_to_f32(uint32_t h) {
-  return DT == 1 ? bf16_bits_to_f32(h) : f16_bits_to_f32(h);
-}
-
-template <int DT, bool VEC>
-__device__ __forceinline__ float elt(const uint4& r, int e) {
-  if constexpr (HCfg<DT, VEC>::kF32Bits) {
-    return __uint_as_float(word_of(r, e));
-  } else {
-    const uint32_t w = word_of(r, e >> 1);
-    return half_to_f32<DT>((e & 1) ? (w >> 16) : (w & 0xFFFFu));
-  }
-}
-
-template <int DT, bool VEC>
-__device__ __forceinline__ uint4 load_unit(const char* row, int32_t u, int32_t V, uint64_t pol) {
-  constexpr int EPU = HCfg<DT, VEC>::kEPU;
-  const int32_t e0 = u * EPU;
-  if constexpr (VEC) {
-    if (e0 + EPU <= V) return ld_stream_v4(row + (size_t)u * 16, pol);
-  }
-  uint32_t w[4];
-  if constexpr (HCfg<DT, VEC>::kF32Bits) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float x = -INFINITY;
-      if (e0 + e < V) {
-        if constexpr (DT == 0)
-          x = __ldg(reinterpret_cast<const float*>(row) + e0 + e);
-        else
-          x = half_to_f32<DT>(__ldg(reinterpret_cast<const unsigned short*>(row) + e0 + e));
-      }
-      w[e] = __float_as_uint(x);
-    }
-  } else {
-    constexpr uint32_t ninf = DT == 1 ? 0xFF80u : 0xFC00u;
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = (e0 + 2 * k < V) ? (uint32_t)__ldg(h + e0 + 2 * k) : ninf;
-      const uint32_t hi = (e0 + 2 * k + 1 < V) ? (uint32_t)__ldg(h + e0 + 2 * k + 1) : ninf;
-      w[k] = lo | (hi << 16);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
+using namespace slice;
 
 constexpr int kHlgThreads = 512;
 constexpr int kHlgWarps = kHlgThreads / 32;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "l"(pol)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
 
 // Online softmax moments of finite logits: M = max x, S = sum e^(x-M),
 // W = sum e^(x-M) x. Empty: M = -inf, S = W = 0.

@@ -55,6 +55,21 @@ struct HlgParams {
   const HlgRowParams* rows;  // per-row curves (device), or nullptr: the fields above
 };
 
+// Categorical baseline launch: one thread-block cluster of `cluster` CTAs per row.
+struct CatParams {
+  const char* logits;
+  int64_t ld_bytes;
+  int64_t B;
+  int32_t V;
+  int32_t units_per_row;
+  int32_t cluster;
+  int32_t units_per_cta;
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  int64_t* out_idx;
+};
+
 // Elements per unit for a dtype code (0 f32, 1 bf16, 2 f16) and load path.
 inline int units_elems(int dtype, bool vec) { return vec ? (dtype == 0 ? 4 : 8) : 4; }
 
@@ -69,6 +84,11 @@ int hlg_max_cluster(int dtype, bool vec, size_t smem_bytes);
 size_t hlg_smem_bytes(int dtype, bool vec, int32_t units_per_cta);
 size_t hlg_smem_limit();
 cudaError_t launch_hlg(const HlgParams& p, int dtype, bool vec, cudaStream_t stream);
+
+// Categorical baseline: largest co-schedulable cluster, per-CTA slice limit.
+int cat_max_cluster(int dtype, bool vec);
+size_t cat_smem_limit();
+cudaError_t launch_categorical(const CatParams& p, int dtype, bool vec, cudaStream_t stream);
 
 cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
                                 int64_t n, uint32_t* out, cudaStream_t stream);
