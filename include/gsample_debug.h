@@ -30,13 +30,23 @@ gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gum
 
 /* gsample_gumbel_argmax / gsample_hlg_gumbel_argmax with an explicit number
  * of CTAs (0 = the library's choice). ctas is clamped to [1, number of 16-byte
- * units in the batch]. hlg == NULL selects the plain sampler. */
+ * units in the batch]. hlg == NULL selects the plain sampler; a positive ctas
+ * then always takes the flat split (sample_kernel), whatever the batch size. */
 gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, int64_t B,
                                        int64_t V, int64_t ld, const float* temperature,
                                        const uint64_t* seed, const uint64_t* offset,
                                        const gsample_hlg_params* hlg, int64_t* out_idx,
                                        void* workspace, int32_t ctas,
                                        gsample_stream_t stream);
+
+/* gsample_gumbel_argmax on the cluster-per-row kernel with `cluster` CTAs per
+ * row (1..16), whatever the batch size (the library picks it for small
+ * batches only). */
+gsample_status gsample_debug_sample_cluster(const void* logits, gsample_dtype dtype, int64_t B,
+                                            int64_t V, int64_t ld, const float* temperature,
+                                            const uint64_t* seed, const uint64_t* offset,
+                                            int64_t* out_idx, void* workspace, int32_t cluster,
+                                            gsample_stream_t stream);
 
 /* gsample_categorical with an explicit cluster size (CTAs per row, 1..16;
  * 0 = the library's choice). */

@@ -34,11 +34,11 @@ def rows_to_device(batch: W.Batch, device="cuda"):
     return T, S, O
 
 
-def gpu_gumbel(batch: W.Batch, logits_dev=None, ctas: int = 0, workspace=None):
+def gpu_gumbel(batch: W.Batch, logits_dev=None, ctas: int = 0, workspace=None, cluster: int = 0):
     torch = torch_mod()
     x = logits_dev if logits_dev is not None else to_device(batch.logits, batch.dtype)
     T, S, O = rows_to_device(batch)
-    out = gs.gumbel_argmax(x, T, S, O, workspace=workspace, ctas=ctas)
+    out = gs.gumbel_argmax(x, T, S, O, workspace=workspace, ctas=ctas, cluster=cluster)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 

@@ -20,8 +20,8 @@ def _oracle_rows(batch, rows=None, kind="gumbel", extra=None):
                             batch.offset, extra=extra, row_ids=rows)
 
 
-def _check_batch(batch, tally=None, rows=None, ctas=0, where=""):
-    gpu = gpu_gumbel(batch, ctas=ctas)
+def _check_batch(batch, tally=None, rows=None, ctas=0, where="", cluster=0):
+    gpu = gpu_gumbel(batch, ctas=ctas, cluster=cluster)
     rows = np.arange(batch.B) if rows is None else np.asarray(rows)
     ref, gap = _oracle_rows(batch, rows)
     t = tally or Tally()
@@ -62,6 +62,25 @@ def test_forced_cta_counts_and_split_ties(dtype, ctas):
     T = np.array([0, 0.7, 0, 1.3, 0, 0.4], np.float32)
     b = W.Batch("ties", W.encode(x, dtype), dtype, T, W.splitmix64(3, B), np.full(B, 5, np.uint64))
     _check_batch(b, ctas=ctas, where="ctas=%d" % ctas)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("cluster", [1, 2, 7, 16])
+def test_cluster_per_row_kernel(dtype, cluster):
+    """The small-batch kernel (one cluster per row) at forced cluster sizes,
+    with the row maximum copied into different CTA slices and lanes, mixed
+    greedy and sampled rows, and a batch larger than it is chosen for."""
+    for B, V in ((6, 20000), (3, 4099), (40, 3000)):
+        rng = np.random.default_rng([cluster, B, V])
+        x = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+        x[rng.random((B, V)) < 0.01] = -np.inf
+        x = W.roundtrip(x, dtype)
+        W.plant_ties(rng, x, range(min(B, 6)))
+        T = rng.uniform(0.3, 2.0, B).astype(np.float32)
+        T[::3] = 0.0
+        b = W.Batch("cluster", W.encode(x, dtype), dtype, T, W.splitmix64(9, B),
+                    np.full(B, 2, np.uint64))
+        _check_batch(b, cluster=cluster, where="cluster=%d B=%d V=%d" % (cluster, B, V))
 
 
 def test_ld_and_misaligned_rows():

@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
             "gsample_categorical": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
             "gsample_debug_categorical_ex": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                     _vp, _i32, _vp]),
+            "gsample_debug_sample_cluster": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                    _vp, _vp, _i32, _vp]),
             "gsample_status_string": (ctypes.c_char_p, [_int]),
             "gsample_debug_philox": (_int, [_u64, _u32, _u64, _i64, _i64, _vp, _vp]),
             "gsample_debug_gumbel": (_int, [_vp, _i64, _vp, _vp, _vp]),
@@ -208,10 +210,13 @@ def argmax(logits, out=None, workspace=None):
     return out
 
 
-def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, ctas: int = 0):
+def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, ctas: int = 0,
+                  cluster: int = 0):
     """Gumbel-max sample per row: argmax_i(logits[i]/T + g_i). temperature
     (float32), seed (uint64 as int64 bits) and offset (uint64 as int64 bits)
-    are per-row tensors or scalars. Rows with T <= 0 are greedy."""
+    are per-row tensors or scalars. Rows with T <= 0 are greedy. Diagnostics:
+    ctas > 0 forces the flat split with that many CTAs; cluster > 0 forces the
+    cluster-per-row kernel with that many CTAs per row."""
     torch = _torch()
     dt, B, V, ld, out, ws = _prepare(logits, out, workspace)
     dev = logits.device
@@ -219,7 +224,11 @@ def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, c
     S = _row_tensor(seed, B, torch.int64, dev, "seed")
     O = _row_tensor(offset, B, torch.int64, dev, "offset")
     L = lib()
-    if ctas:
+    if cluster:
+        st = L.gsample_debug_sample_cluster(logits.data_ptr(), dt, B, V, ld, T.data_ptr(),
+                                            S.data_ptr(), O.data_ptr(), out.data_ptr(),
+                                            ws.data_ptr(), cluster, _stream_ptr(dev))
+    elif ctas:
         st = L.gsample_debug_sample_ex(logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(),
                                        O.data_ptr(), None, out.data_ptr(), ws.data_ptr(), ctas,
                                        _stream_ptr(dev))

@@ -6,7 +6,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "gsample.h"
 #include "gsample_debug.h"
@@ -16,7 +18,7 @@ namespace {
 
 using gsample::SampleParams;
 using gsample::HlgParams;
-using gsample::CatParams;
+using gsample::RowClusterParams;
 using gsample::WsRow;
 
 // Largest V: element indices, Philox group indices and the packed key's low
@@ -33,6 +35,7 @@ struct DeviceInfo {
   int sample_slots[6] = {0, 0, 0, 0, 0, 0};  // CTAs per SM, per (dtype, vec)
   int hlg_cluster[6] = {0, 0, 0, 0, 0, 0};   // largest co-schedulable cluster, per (dtype, vec)
   int cat_cluster[6] = {0, 0, 0, 0, 0, 0};   // the same for the categorical baseline
+  int rc_cluster[6] = {0, 0, 0, 0, 0, 0};    // the same for the small-batch sampler
 };
 
 std::mutex g_mu;
@@ -77,6 +80,12 @@ gsample_status device_info(const DeviceInfo** out) {
             return GSAMPLE_ERR_CUDA;
           }
           d.cat_cluster[dt * 2 + v] = cc;
+          const int rc = gsample::rc_max_cluster(dt, v != 0);
+          if (rc <= 0) {
+            cudaGetLastError();
+            return GSAMPLE_ERR_CUDA;
+          }
+          d.rc_cluster[dt * 2 + v] = rc;
         }
     }
     d.ready = true;
@@ -86,6 +95,70 @@ gsample_status device_info(const DeviceInfo** out) {
 }
 
 int64_t elt_bytes(gsample_dtype dt) { return dt == GSAMPLE_F32 ? 4 : 2; }
+
+// How many clusters of `cluster` CTAs of `fn` (with `smem` bytes of dynamic
+// shared memory each) the device runs at once; cached per device, kernel,
+// cluster size and 16 KB step of shared memory.
+int active_clusters(void* fn, int threads, int cluster, size_t smem) {
+  static std::map<std::tuple<int, void*, int, size_t>, int> cache;
+  const size_t bucket = (smem + 16383) / 16384;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, fn, cluster, bucket);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = bucket * 16384;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  cache[key] = n;
+  return n;
+}
+
+// The cluster size for B rows of `nu` units: the largest size (at most
+// max_cluster, and no more CTAs than nu / min_units) whose clusters all run in
+// one wave; if none does, the one that runs the most rows at a time per CTA.
+int pick_cluster(void* (*kernel)(int, bool, bool, int*), int dtype, bool vec, int64_t B,
+                 int64_t nu, int max_cluster, int64_t min_units, size_t smem_limit) {
+  int64_t cap = (nu + min_units - 1) / min_units;
+  if (cap < 1) cap = 1;
+  int top = max_cluster < 1 ? 1 : max_cluster;
+  if (top > cap) top = (int)cap;
+  int best = top;
+  double best_rate = -1.0;
+  for (int c = top; c >= 1; --c) {
+    const size_t smem = (size_t)((nu + c - 1) / c) * 16;
+    const bool resident = smem <= smem_limit;
+    int threads = 0;
+    void* fn = kernel(dtype, vec, resident, &threads);
+    const int n = active_clusters(fn, threads, c, resident ? smem : 0);
+    if (n <= 0) continue;
+    if (B <= n) return c;  // one wave
+    // rows finished per unit of time, if time per row scales with units per CTA
+    const double rate = (double)n * c;
+    if (rate > best_rate) {
+      best_rate = rate;
+      best = c;
+    }
+  }
+  return best;
+}
 
 gsample_status check_common(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
                             int64_t ld, const int64_t* out_idx, const void* ws,
@@ -137,15 +210,56 @@ void plan_sample(const DeviceInfo& d, const void* logits, gsample_dtype dtype, i
   *vec_out = vec;
 }
 
+// Batches of at most this many rows take the cluster-per-row kernel; a CTA of
+// it gets at least this many units.
+constexpr int64_t kClusterMaxRows = 16;
+constexpr int64_t kClusterUnitsPerCta = 512;
+
 gsample_status run_sample(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
                           int64_t ld, const float* temperature, const uint64_t* seed,
                           const uint64_t* offset, int64_t* out_idx, void* workspace,
-                          int32_t ctas_override, cudaStream_t stream) {
+                          int32_t ctas_override, cudaStream_t stream,
+                          int32_t cluster_override = 0) {
   gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
   if (st != GSAMPLE_OK || B == 0) return st;
   const DeviceInfo* d = nullptr;
   st = device_info(&d);
   if (st != GSAMPLE_OK) return st;
+  if (ctas_override == 0 || cluster_override > 0) {
+    // Small batches: one cluster per row (latency-bound sizes), unless a CTA
+    // count for the flat split was asked for.
+    const bool vec = vec_path(logits, dtype, ld);
+    const int epu = gsample::units_elems((int)dtype, vec);
+    const int64_t nu = (V + epu - 1) / epu;
+    const int max_cluster = d->rc_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
+    int cluster = cluster_override;
+    if (cluster == 0 && B <= kClusterMaxRows) {
+      cluster = pick_cluster(gsample::rc_kernel, (int)dtype, vec, B, nu, max_cluster,
+                             kClusterUnitsPerCta, gsample::rc_smem_limit());
+      if ((nu + cluster - 1) / cluster * 16 > (int64_t)gsample::rc_smem_limit()) cluster = 0;
+    }
+    if (cluster > 0) {
+      if (cluster > 16 || cluster > max_cluster) return GSAMPLE_ERR_INVALID_ARG;
+      RowClusterParams q;
+      std::memset(&q, 0, sizeof q);
+      q.logits = static_cast<const char*>(logits);
+      q.ld_bytes = ld * elt_bytes(dtype);
+      q.B = B;
+      q.V = (int32_t)V;
+      q.units_per_row = (int32_t)nu;
+      q.cluster = cluster;
+      q.units_per_cta = (int32_t)((nu + cluster - 1) / cluster);
+      q.temperature = temperature;
+      q.seed = seed;
+      q.offset = offset;
+      q.out_idx = out_idx;
+      if (gsample::launch_sample_cluster(q, (int)dtype, vec, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GSAMPLE_ERR_CUDA;
+      }
+      return GSAMPLE_OK;
+    }
+  }
   SampleParams p;
   bool vec = false;
   plan_sample(*d, logits, dtype, B, V, ld, ctas_override, &p, &vec);
@@ -178,14 +292,11 @@ gsample_status run_categorical(const void* logits, gsample_dtype dtype, int64_t 
   const int64_t nu = (V + epu - 1) / epu;
   const int max_cluster = d->cat_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
   int cluster = cluster_override;
-  if (cluster == 0) {
-    cluster = max_cluster < 1 ? 1 : max_cluster;
-    int64_t cap = (nu + gsample::kThreads - 1) / gsample::kThreads;
-    if (cap < 1) cap = 1;
-    if (cluster > cap) cluster = (int)cap;
-  }
+  if (cluster == 0)
+    cluster = pick_cluster(gsample::cat_kernel, (int)dtype, vec, B, nu, max_cluster,
+                           gsample::kThreads, gsample::cat_smem_limit());
   if (cluster < 1 || cluster > 16 || cluster > max_cluster) return GSAMPLE_ERR_INVALID_ARG;
-  CatParams p;
+  RowClusterParams p;
   std::memset(&p, 0, sizeof p);
   p.logits = static_cast<const char*>(logits);
   p.ld_bytes = ld * elt_bytes(dtype);
@@ -238,15 +349,10 @@ gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64
   // Smallest cluster whose CTAs can each hold their slice of the row on chip;
   // if even the largest cluster cannot, the slices stream from memory twice.
   int cluster = ctas_override > 0 ? ctas_override : 0;
-  if (cluster == 0) {
-    const int max_cluster = d->hlg_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
-    cluster = max_cluster < 1 ? 1 : max_cluster;
-    // Prefer spreading a row over the whole cluster when B is small (latency),
-    // but never more CTAs per row than units / threads.
-    int64_t cap = (nu + gsample::kThreads - 1) / gsample::kThreads;
-    if (cap < 1) cap = 1;
-    if (cluster > cap) cluster = (int)cap;
-  }
+  if (cluster == 0)
+    cluster = pick_cluster(gsample::hlg_kernel_fn, (int)dtype, vec, B, nu,
+                           d->hlg_cluster[(int)dtype * 2 + (vec ? 1 : 0)], gsample::kThreads,
+                           gsample::hlg_smem_limit());
   if (cluster > 16 || cluster > d->hlg_cluster[(int)dtype * 2 + (vec ? 1 : 0)])
     return GSAMPLE_ERR_INVALID_ARG;
   HlgParams p;
@@ -402,6 +508,17 @@ gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, 
   if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
   return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, ctas,
                     (cudaStream_t)stream);
+}
+
+gsample_status gsample_debug_sample_cluster(const void* logits, gsample_dtype dtype, int64_t B,
+                                            int64_t V, int64_t ld, const float* temperature,
+                                            const uint64_t* seed, const uint64_t* offset,
+                                            int64_t* out_idx, void* workspace, int32_t cluster,
+                                            gsample_stream_t stream) {
+  if (cluster < 1) return GSAMPLE_ERR_INVALID_ARG;
+  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
+  return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
+                    (cudaStream_t)stream, cluster);
 }
 
 gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dtype, int64_t B,

@@ -56,7 +56,7 @@ struct CatPart {
 };
 
 template <int DT, bool VEC, bool RESIDENT>
-__global__ void __launch_bounds__(kCatThreads) categorical_kernel(const CatParams p) {
+__global__ void __launch_bounds__(kCatThreads) categorical_kernel(const RowClusterParams p) {
   using C = HCfg<DT, VEC>;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ CatPart s_part;  // read by the whole cluster
@@ -343,6 +343,11 @@ constexpr size_t kCatSmemLimit = 200 * 1024;  // leaves room for the static shar
 
 size_t cat_smem_limit() { return kCatSmemLimit; }
 
+void* cat_kernel(int dtype, bool vec, bool resident, int* threads) {
+  *threads = kCatThreads;
+  return select_cat(dtype, vec, resident);
+}
+
 // One-time per-device setup (as for the HLG kernel): allow clusters of up to
 // 16 CTAs and the full slice, then report the largest co-schedulable cluster.
 int cat_max_cluster(int dtype, bool vec) {
@@ -371,7 +376,7 @@ int cat_max_cluster(int dtype, bool vec) {
   return size;
 }
 
-cudaError_t launch_categorical(const CatParams& p, int dtype, bool vec, cudaStream_t stream) {
+cudaError_t launch_categorical(const RowClusterParams& p, int dtype, bool vec, cudaStream_t stream) {
   const size_t need = (size_t)p.units_per_cta * 16;
   const bool resident = need <= kCatSmemLimit;
   void* fn = select_cat(dtype, vec, resident);
@@ -387,7 +392,7 @@ cudaError_t launch_categorical(const CatParams& p, int dtype, bool vec, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {const_cast<CatParams*>(&p)};
+  void* args[] = {const_cast<RowClusterParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

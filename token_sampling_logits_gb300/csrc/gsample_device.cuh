@@ -278,6 +278,38 @@ __device__ __forceinline__ Prune make_prune(float L, float T) {
 }
 
 // ---------------------------------------------------------------------------
+// Exact scores of the sampled path: s = x / T (IEEE division) + g(word).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exact_score(float x, uint32_t word, float T) {
+  return x == INFINITY ? INFINITY : __fdiv_rn(x, T) + gumbel_of_word(word);
+}
+
+// Rare path: the element-wise test, then the exact score.
+__device__ __forceinline__ void score_group(uint32_t gid, float x0, float x1, float x2, float x3,
+                                         uint4 w, Prune pr, ReachTest rt, float T, float* bs_io,
+                                         int32_t* bi_io) {
+  const float x[4] = {x0, x1, x2, x3};
+  float bs = *bs_io;
+  int32_t bi = *bi_io;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t wd = word_of(w, t);
+    const bool need = pr.use_bound ? may_reach(x[t], wd, rt) : (x[t] >= pr.thr_x);
+    if (need) take_better(exact_score(x[t], wd, T), (int32_t)(4 * gid + t), bs, bi);
+  }
+  *bs_io = bs;
+  *bi_io = bi;
+}
+
+// Can the group still reach L, given its largest logit and largest Philox word
+// (v = 1 - u only shrinks as the word grows, so one test covers all four)?
+__device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const Prune& pr,
+                                                const ReachTest& rt) {
+  if (!pr.use_bound) return xm >= pr.thr_x;
+  return may_reach(xm, max(max(w.x, w.y), max(w.z, w.w)), rt);
+}
+
+// ---------------------------------------------------------------------------
 // Loads. Logit rows are read exactly once, so the 128-bit loads go through the
 // non-coherent path, skip L1 allocation and carry an L2 evict-first policy.
 // ---------------------------------------------------------------------------

@@ -417,6 +417,11 @@ constexpr size_t kSmemLimit = 224 * 1024;  // leaves room for the static shared 
 
 size_t hlg_smem_limit() { return kSmemLimit; }
 
+void* hlg_kernel_fn(int dtype, bool vec, bool resident, int* threads) {
+  *threads = kHlgThreads;
+  return select_hlg(dtype, vec, resident);
+}
+
 size_t hlg_smem_bytes(int, bool, int32_t units_per_cta) { return (size_t)units_per_cta * 16; }
 
 // One-time per-device setup of both variants of (dtype, vec): allow clusters

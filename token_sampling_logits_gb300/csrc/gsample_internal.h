@@ -55,8 +55,9 @@ struct HlgParams {
   const HlgRowParams* rows;  // per-row curves (device), or nullptr: the fields above
 };
 
-// Categorical baseline launch: one thread-block cluster of `cluster` CTAs per row.
-struct CatParams {
+// Launches with one thread-block cluster of `cluster` CTAs per row (the
+// categorical baseline and the small-batch sampler).
+struct RowClusterParams {
   const char* logits;
   int64_t ld_bytes;
   int64_t B;
@@ -85,10 +86,23 @@ size_t hlg_smem_bytes(int dtype, bool vec, int32_t units_per_cta);
 size_t hlg_smem_limit();
 cudaError_t launch_hlg(const HlgParams& p, int dtype, bool vec, cudaStream_t stream);
 
+// The cluster-per-row kernels of (dtype, vec, resident) and their block size,
+// for occupancy queries.
+void* rc_kernel(int dtype, bool vec, bool resident, int* threads);
+void* cat_kernel(int dtype, bool vec, bool resident, int* threads);
+void* hlg_kernel_fn(int dtype, bool vec, bool resident, int* threads);
+
+// Small-batch sampler (one cluster per row): largest co-schedulable cluster,
+// per-CTA slice limit, launch.
+int rc_max_cluster(int dtype, bool vec);
+size_t rc_smem_limit();
+cudaError_t launch_sample_cluster(const RowClusterParams& p, int dtype, bool vec,
+                                  cudaStream_t stream);
+
 // Categorical baseline: largest co-schedulable cluster, per-CTA slice limit.
 int cat_max_cluster(int dtype, bool vec);
 size_t cat_smem_limit();
-cudaError_t launch_categorical(const CatParams& p, int dtype, bool vec, cudaStream_t stream);
+cudaError_t launch_categorical(const RowClusterParams& p, int dtype, bool vec, cudaStream_t stream);
 
 cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
                                 int64_t n, uint32_t* out, cudaStream_t stream);
