@@ -212,7 +212,7 @@ void plan_sample(const DeviceInfo& d, const void* logits, gsample_dtype dtype, i
 
 // Batches of at most this many rows take the cluster-per-row kernel; a CTA of
 // it gets at least this many units.
-constexpr int64_t kClusterMaxRows = 16;
+constexpr int64_t kClusterMaxRows = 64;
 constexpr int64_t kClusterUnitsPerCta = 512;
 
 gsample_status run_sample(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
