@@ -123,3 +123,19 @@ def test_per_row_hlg_entry_validation():
     assert call(rows=FAKE + 2) == gs.ERR_INVALID_ARG   # 24-byte records of 4-byte fields
     assert call(out=None) == gs.ERR_INVALID_ARG
     assert call(logits=None) == gs.ERR_INVALID_ARG
+
+
+def test_categorical_entry_validation():
+    L = gs.lib()
+
+    def call(B=4, logits=FAKE, T=FAKE, out=FAKE):
+        return L.gsample_categorical(logits, gs.F32, B, 100, 100, T, FAKE, FAKE, out, None)
+
+    assert call(B=0) == gs.OK                      # empty batch: nothing to do
+    assert call(logits=None) == gs.ERR_INVALID_ARG
+    assert call(out=None) == gs.ERR_INVALID_ARG
+    assert call(T=None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_categorical_ex(FAKE, gs.F32, 4, 100, 100, FAKE, FAKE, FAKE, FAKE, -1,
+                                          None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_sample_cluster(FAKE, gs.F32, 4, 100, 100, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                          0, None) == gs.ERR_INVALID_ARG
