@@ -45,13 +45,19 @@ namespace {
 #define GSAMPLE_VPT 8
 #endif
 #ifndef GSAMPLE_STAGES
-#define GSAMPLE_STAGES 3
+#define GSAMPLE_STAGES 2
 #endif
 #ifndef GSAMPLE_MIN_CTAS_PER_SM
 #define GSAMPLE_MIN_CTAS_PER_SM 2
 #endif
 constexpr int kVPT = GSAMPLE_VPT;        // units per lane per tile
 constexpr int kStages = GSAMPLE_STAGES;  // tiles per warp ring
+
+// The rare list of a warp: 32 entries of a row-local group index (4 bytes)
+// and the group's four logits as stored in the tile (at most 16 bytes).
+constexpr int kRareCap = 32;
+constexpr uint32_t kRareRawOff = kRareCap * 4;  // byte offset of the logits array
+constexpr int kRareBytes = (int)kRareRawOff + kRareCap * 16;
 
 template <int DT, bool VEC>
 struct Cfg {
@@ -64,7 +70,9 @@ struct Cfg {
   // 4-element scalar path) or raw 16-bit values (bf16/f16 on the 128-bit path).
   static constexpr bool kF32Bits = DT == 0 || !VEC;
   static constexpr int kTileBytes = kTile * 16;
-  static constexpr int kListBytes = ((kCap * (kF32Bits ? 8 : 4) + 15) / 16) * 16;
+  // A warp's list area: the rare list, then a tile's compacted list (one
+  // 16-bit tile-local group index per surviving group).
+  static constexpr int kListBytes = ((kRareBytes + kCap * 2 + 15) / 16) * 16;
   static constexpr int kWarpBytes = kStages * kTileBytes + kListBytes;
   static constexpr size_t kSmem = (size_t)kWarps * kWarpBytes;
 };
@@ -307,16 +315,6 @@ __device__ __noinline__ void finish_row_if_last(const SampleParams& p, int64_t b
 // until 32 of them (or the end of the warp's part of the row) make one exact
 // pass with every lane busy. An entry holds the row-local group index and the
 // group's four logits as stored in the tile (so the ring stage may be reused).
-constexpr int kRareCap = 32;
-constexpr uint32_t kRareRawOff = kRareCap * 4;  // byte offset of the logits array
-// A warp's list area holds the rare list, then the compacted list of a tile
-// (one 16-bit tile-local group index per surviving group).
-constexpr int kRareBytes = (int)kRareRawOff + kRareCap * 16;
-static_assert(kRareBytes + Cfg<0, true>::kCap * 2 <= Cfg<0, true>::kListBytes &&
-                  kRareBytes + Cfg<1, true>::kCap * 2 <= Cfg<1, true>::kListBytes &&
-                  kRareBytes + Cfg<1, false>::kCap * 2 <= Cfg<1, false>::kListBytes,
-              "the rare list and a tile's compacted list must fit in a warp's list area");
-
 template <int DT, bool VEC>
 using RareRaw = typename std::conditional<Cfg<DT, VEC>::kF32Bits, uint4, uint2>::type;
 
