@@ -53,7 +53,17 @@ def parse_args():
     ap.add_argument("--quick", action="store_true",
                     help="headline timing only (no CPU baseline, e2e, clocks or table); for "
                          "profiler runs")
-    return ap.parse_args()
+    ap.add_argument("--workload", choices=["throughput", "sweep", "hlg", "mixed_greedy"],
+                    default="throughput",
+                    help="with --quick: time this workload instead of the headline (sweep takes "
+                         "--batch and --vocab); prints a short line, for profiler runs")
+    ap.add_argument("--vocab", type=int, default=151936, help="V of --workload sweep")
+    ap.add_argument("--categorical", action="store_true",
+                    help="with --workload: time the categorical (softmax + inverse-CDF) kernel")
+    args = ap.parse_args()
+    if (args.workload != "throughput" or args.categorical) and not args.quick:
+        ap.error("--workload and --categorical time a side case and need --quick")
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -382,55 +392,92 @@ def time_steps(runner: Runner, steps: int, warmup: int, dist: Dist, clocks: Cloc
     return ms, clk
 
 
-def e2e_steps(batch: W.Batch, steps: int, dist: Dist):
-    """Same metric through the public API with host buffers: every step copies
-    its logits and per-row parameters from pinned host memory, samples, and
-    copies the indices back."""
+def _pinned_batch_copies(batch: W.Batch, n: int):
+    import torch
+
+    if batch.dtype == W.F32:
+        base = torch.from_numpy(np.ascontiguousarray(batch.logits, dtype=np.float32))
+        view = lambda t: t  # noqa: E731
+    else:
+        base = torch.from_numpy(np.ascontiguousarray(batch.logits).view(np.int16))
+        tdt = torch.bfloat16 if batch.dtype == W.BF16 else torch.float16
+        view = lambda t: t.view(tdt)  # noqa: E731
+    return [view(base.clone().pin_memory()) for _ in range(n)]
+
+
+def e2e_steps(batch: W.Batch, steps: int, dist: Dist, l2: int):
+    """Same metric through the public API with host buffers. Each step the
+    sampler reads its logits and per-row parameters from pinned host memory
+    over the CPU-GPU link and writes the indices into pinned host memory
+    (the C ABI's gsample_gumbel_argmax_host: no staging copy); the host waits
+    for them.
+    Steps rotate over host buffers larger than 2x L2, so no step finds its
+    logits cached. Also timed: the staged path (cudaMemcpyAsync of the inputs
+    into device buffers, gsample_gumbel_argmax, copy of the indices back).
+    Both call the C ABI directly, as a C caller would."""
     import torch
 
     import token_sampling_logits_gb300 as gs
 
     B = batch.B
-    if batch.dtype == W.F32:
-        h_x = torch.from_numpy(np.ascontiguousarray(batch.logits)).pin_memory()
-    else:
-        h_x = torch.from_numpy(np.ascontiguousarray(batch.logits).view(np.int16)).pin_memory()
+    nbytes = batch.logits.size * (4 if batch.dtype == W.F32 else 2)
+    n_buf = max(2, math.ceil(2 * l2 / nbytes) + 1)
+    h_x = _pinned_batch_copies(batch, n_buf)
     h_T = torch.from_numpy(batch.temperature.astype(np.float32)).pin_memory()
     h_S = torch.from_numpy(batch.seed.view(np.int64).copy()).pin_memory()
     h_O = torch.zeros(B, dtype=torch.int64).pin_memory()
     h_out = torch.zeros(B, dtype=torch.int64).pin_memory()
-    d_x = torch.empty(h_x.shape, dtype=h_x.dtype, device="cuda")
+    ws = gs.new_workspace(B)
+    h2d = nbytes + B * (4 + 8 + 8)
+    d2h = B * 8
+
+    L = gs.lib()
+    dt = {W.F32: gs.F32, W.BF16: gs.BF16, W.F16: gs.F16}[batch.dtype]
+    V = ld = batch.V
+    stream = torch.cuda.current_stream()
+
+    def step_mapped(k):
+        h_O.fill_(k)
+        rc = L.gsample_gumbel_argmax_host(h_x[k % n_buf].data_ptr(), dt, B, V, ld,
+                                          h_T.data_ptr(), h_S.data_ptr(), h_O.data_ptr(),
+                                          h_out.data_ptr(), ws.data_ptr(), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError("gsample_gumbel_argmax_host: " + gs.status_string(rc))
+        stream.synchronize()  # the caller reads the tokens
+
+    d_x = torch.empty(h_x[0].shape, dtype=h_x[0].dtype, device="cuda")
     d_T = torch.empty(B, dtype=torch.float32, device="cuda")
     d_S = torch.empty(B, dtype=torch.int64, device="cuda")
     d_O = torch.empty(B, dtype=torch.int64, device="cuda")
     d_out = torch.empty(B, dtype=torch.int64, device="cuda")
-    ws = gs.new_workspace(B)
-    view = (lambda t: t) if batch.dtype == W.F32 else (
-        lambda t: t.view(torch.bfloat16 if batch.dtype == W.BF16 else torch.float16))
-    h2d = h_x.numel() * h_x.element_size() + B * (4 + 8 + 8)
-    d2h = B * 8
 
-    def step(k):
+    def step_staged(k):
         h_O.fill_(k)
-        d_x.copy_(h_x, non_blocking=True)
+        d_x.copy_(h_x[k % n_buf], non_blocking=True)
         d_T.copy_(h_T, non_blocking=True)
         d_S.copy_(h_S, non_blocking=True)
         d_O.copy_(h_O, non_blocking=True)
-        gs.gumbel_argmax(view(d_x), d_T, d_S, d_O, out=d_out, workspace=ws)
+        rc = L.gsample_gumbel_argmax(d_x.data_ptr(), dt, B, V, ld, d_T.data_ptr(), d_S.data_ptr(),
+                                     d_O.data_ptr(), d_out.data_ptr(), ws.data_ptr(),
+                                     stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError("gsample_gumbel_argmax: " + gs.status_string(rc))
         h_out.copy_(d_out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()  # the caller reads the tokens
+        stream.synchronize()  # the caller reads the tokens
 
-    for k in range(3):
-        step(k)
-    dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for k in range(steps):
-        step(k)
-    torch.cuda.synchronize()
-    secs = time.perf_counter() - t0
-    dist.barrier()
-    return secs, h2d, d2h
+    secs = {}
+    for name, step in (("mapped", step_mapped), ("staged", step_staged)):
+        for k in range(3):
+            step(k)
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in range(steps):
+            step(k)
+        torch.cuda.synchronize()
+        secs[name] = time.perf_counter() - t0
+        dist.barrier()
+    return secs, h2d, d2h, n_buf
 
 
 def extra_table(dist: Dist, l2: int):
@@ -467,6 +514,39 @@ def extra_table(dist: Dist, l2: int):
             row["categorical_over_gumbel"] = round(cu / us, 3)
         rows.append(row)
     return rows
+
+
+def run_case(args):
+    """One side workload (--quick --workload ...), graph-replayed over a pool
+    larger than 4x L2, for capturing its kernel under a profiler."""
+    import torch
+
+    import token_sampling_logits_gb300 as gs
+
+    gs.lib()
+    hp = None
+    if args.workload == "sweep":
+        b = W.sweep(args.vocab, args.batch)
+    elif args.workload == "hlg":
+        b = W.hlg()
+        p = W.HLG_PARAMS
+        hp = gs.HlgParams(m=p["m"], w=p["w"], beta_t=p["beta_t"], beta_h=p["beta_h"],
+                          pivot_offset=p["c"])
+    elif args.workload == "mixed_greedy":
+        b = W.mixed_greedy()
+    else:
+        b = W.throughput(args.batch)
+    if hp is not None and args.categorical:
+        raise SystemExit("--categorical has no HLG form")
+    props = torch.cuda.get_device_properties(0)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    r = Runner(b, hlg=hp, min_pool_bytes=4 * l2, ring=max(1, args.steps),
+               categorical=args.categorical)
+    ms, _ = time_steps(r, args.steps, max(3, args.warmup), Dist(1))
+    print(json.dumps({"workload": args.workload, "B": b.B, "V": b.V,
+                      "dtype": W.DTYPE_NAMES[b.dtype], "categorical": args.categorical,
+                      "steps": args.steps, "us_per_step": round(ms * 1000 / args.steps, 3)}),
+          flush=True)
 
 
 def run_ours(args, dist: Dist):
@@ -521,10 +601,16 @@ def run_ours(args, dist: Dist):
 
     e2e = None
     if not args.quick:
-        e2e_secs, h2d, d2h = e2e_steps(batch, args.e2e_steps, dist)
-        e2e_secs = dist.max(e2e_secs)
-        e2e = {"value": round(batch.B * args.e2e_steps * dist.world / e2e_secs, 1),
-               "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        secs, h2d, d2h, n_buf = e2e_steps(batch, args.e2e_steps, dist, l2)
+        rows_e2e = batch.B * args.e2e_steps * dist.world
+        e2e = {"value": round(rows_e2e / dist.max(secs["mapped"]), 1),
+               "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "gsample_gumbel_argmax_host: the kernel reads pinned host logits and "
+                       "parameters over the CPU-GPU link and writes the indices to pinned host "
+                       "memory; %d host buffers in rotation" % n_buf,
+               "staged_value": round(rows_e2e / dist.max(secs["staged"]), 1),
+               "staged_path": "cudaMemcpyAsync of the inputs to device buffers, "
+                              "gsample_gumbel_argmax, copy of the indices back"}
 
     extra = None if args.no_extra or args.quick or dist.rank != 0 else extra_table(Dist(1), l2)
 
@@ -615,6 +701,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, dist)
+        elif args.workload != "throughput" or args.categorical:
+            run_case(args)
         else:
             run_ours(args, dist)
     finally:

@@ -194,6 +194,30 @@ gsample_status gsample_gumbel_argmax_static(const void* logits, gsample_dtype dt
                                             const uint64_t* seed, const uint64_t* offset,
                                             int64_t* out_idx, gsample_stream_t stream);
 
+/* gsample_gumbel_argmax on host-resident data, with no staging copy: logits,
+ * temperature, seed, offset and out_idx are page-locked HOST buffers
+ * (cudaHostAlloc / cudaMallocHost, or cudaHostRegister), which the kernel
+ * reads and writes through their mapping into the current device. On a GB300
+ * the loads cross the CPU-GPU link once per logit; no device copy of the
+ * logits is made. workspace stays a DEVICE buffer.
+ *   - Each of the five host pointers is looked up with cudaPointerGetAttributes.
+ *     One that is not page-locked host memory mapped into the current device
+ *     returns GSAMPLE_ERR_INVALID_ARG, a workspace that is not device memory
+ *     GSAMPLE_ERR_WORKSPACE; nothing is enqueued in either case. Buffer sizes
+ *     cannot be checked: the caller guarantees B rows of ld elements, and B
+ *     entries of the per-row arrays.
+ *   - Asynchronous on `stream`: out_idx holds the indices once `stream` has been
+ *     synchronised, and the host must not write the inputs before then.
+ *   - Shapes, ld, alignment, NaN/inf handling, greedy rows and the workspace
+ *     contract are those of gsample_gumbel_argmax, and so are the indices.
+ *   - Its rate is the link's (host-to-device reads measured about 0.21 TB/s on
+ *     GB300, the same as cudaMemcpyAsync), not the kernel's. */
+gsample_status gsample_gumbel_argmax_host(const void* logits, gsample_dtype dtype, int64_t B,
+                                          int64_t V, int64_t ld, const float* temperature,
+                                          const uint64_t* seed, const uint64_t* offset,
+                                          int64_t* out_idx, void* workspace,
+                                          gsample_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -139,3 +139,21 @@ def test_categorical_entry_validation():
                                           None) == gs.ERR_INVALID_ARG
     assert L.gsample_debug_sample_cluster(FAKE, gs.F32, 4, 100, 100, FAKE, FAKE, FAKE, FAKE, FAKE,
                                           0, None) == gs.ERR_INVALID_ARG
+
+
+def test_host_buffer_entry_validation():
+    L = gs.lib()
+
+    def call(B=4, logits=FAKE, T=FAKE, out=FAKE, ws=FAKE):
+        return L.gsample_gumbel_argmax_host(logits, gs.F32, B, 100, 100, T, FAKE, FAKE, out, ws,
+                                            None)
+
+    assert call(B=0) == gs.OK                       # empty batch: nothing to do
+    assert call(logits=None) == gs.ERR_INVALID_ARG
+    assert call(T=None) == gs.ERR_INVALID_ARG
+    assert call(out=FAKE + 4) == gs.ERR_INVALID_ARG
+    assert call(ws=None) == gs.ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        # the pointer checks need the device: without one the call fails loudly
+        assert call() == gs.ERR_CUDA

@@ -96,3 +96,16 @@ def test_integer_pipe_peak_from_unit_counts():
         mhz = 2070.0
     assert peak == pytest.approx(152 * mhz * 1e6 * 64 / 2 / 18, rel=1e-9)
     assert kind.startswith("derived")
+
+
+def test_side_workload_needs_quick(monkeypatch):
+    b = _bench()
+    monkeypatch.setattr("sys.argv", ["bench.py", "--quick", "--workload", "sweep", "--batch", "8"])
+    a = b.parse_args()
+    assert (a.workload, a.batch, a.vocab, a.categorical) == ("sweep", 8, 151936, False)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--workload", "hlg"])
+    with pytest.raises(SystemExit):
+        b.parse_args()  # a side case never replaces the headline line
+    monkeypatch.setattr("sys.argv", ["bench.py", "--categorical"])
+    with pytest.raises(SystemExit):
+        b.parse_args()

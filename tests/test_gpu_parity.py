@@ -101,6 +101,29 @@ def test_ld_and_misaligned_rows():
             Tally().add(got, ref, gap, greedy_mask=~(T > 0), where="shift=%d dt=%d" % (shift, dtype))
 
 
+@pytest.mark.parametrize("ctas", [3, 40, 400])
+def test_flat_split_on_rows_off_128_byte_lines(ctas):
+    """The flat split moves each warp's split point down to a unit that starts a
+    128-byte line of its row. Here the row stride is 8144 bytes, so successive
+    rows start at every 16-byte offset within a line, and the base pointer is
+    shifted by 0..112 bytes; with 400 CTAs the warps' ranges shrink to 8 units."""
+    B, V = 11, 4000
+    rng = np.random.default_rng(ctas)
+    base = (rng.standard_normal((B, V + 72)) * 2).astype(np.float32)
+    enc = W.encode(base, W.BF16)
+    dev = to_device(enc, W.BF16)
+    T = rng.uniform(0.3, 2.0, B).astype(np.float32)
+    T[::3] = 0.0
+    for shift in (0, 8, 24, 56):  # elements: 0, 16, 48 and 112 bytes
+        view = dev[:, shift:shift + V]
+        host = np.ascontiguousarray(enc[:, shift:shift + V])
+        b = W.Batch("lines", host, W.BF16, T, W.splitmix64(ctas, B), np.full(B, shift, np.uint64))
+        Tt, S, O = rows_to_device(b)
+        got = gs.gumbel_argmax(view, Tt, S, O, ctas=ctas).cpu().numpy()
+        ref, gap = _oracle_rows(b)
+        Tally().add(got, ref, gap, greedy_mask=~(T > 0), where="ctas=%d shift=%d" % (ctas, shift))
+
+
 def test_special_values():
     B, V = 8, 777
     x = np.random.default_rng(2).standard_normal((B, V)).astype(np.float32)

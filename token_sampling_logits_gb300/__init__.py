@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
             "gsample_debug_planned_ctas": (_i32, [_int, _i64, _i64, _i64, _vp, _i32]),
             "gsample_gumbel_argmax_static": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                     _vp, _vp]),
+            "gsample_gumbel_argmax_host": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                  _vp, _vp, _vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -236,6 +238,54 @@ def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, c
         st = L.gsample_gumbel_argmax(logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(),
                                      O.data_ptr(), out.data_ptr(), ws.data_ptr(), _stream_ptr(dev))
     _check(st, "gsample_gumbel_argmax")
+    return out
+
+
+def _pinned_row(x, B, dtype, name):
+    torch = _torch()
+    if not torch.is_tensor(x):
+        x = torch.full((B,), x, dtype=dtype).pin_memory()
+    if x.dtype != dtype or x.is_cuda or x.shape != (B,) or not x.is_contiguous() or \
+            not x.is_pinned():
+        raise ValueError("%s must be a contiguous pinned %s host tensor of shape [%d]" %
+                         (name, dtype, B))
+    return x
+
+
+def gumbel_argmax_host(logits, temperature, seed, offset, out=None, workspace=None,
+                       sync: bool = True):
+    """gumbel_argmax on pinned HOST tensors: the kernel reads the logits and the
+    per-row arrays over the CPU-GPU link and writes the indices straight into
+    `out` (a pinned int64 host tensor), with no device copy of the logits. The
+    workspace is a device tensor. With sync=False the call only enqueues on the
+    current CUDA stream, and `out` is ready once that stream is synchronised."""
+    torch = _torch()
+    if logits.is_cuda or not logits.is_pinned():
+        raise ValueError("logits must be a pinned host tensor")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D [B, V] with contiguous rows")
+    dt = _dtype_code(logits)
+    B, V = logits.shape
+    ld = logits.stride(0) if B > 1 else V
+    T = _pinned_row(temperature, B, torch.float32, "temperature")
+    S = _pinned_row(seed, B, torch.int64, "seed")
+    O = _pinned_row(offset, B, torch.int64, "offset")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64).pin_memory()
+    else:
+        _pinned_row(out, B, torch.int64, "out")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = new_workspace(B, dev)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < workspace_bytes(B):
+        raise ValueError("workspace must be a device tensor of at least workspace_bytes(B) bytes")
+    stream = torch.cuda.current_stream(dev)
+    _check(lib().gsample_gumbel_argmax_host(logits.data_ptr(), dt, B, V, ld, T.data_ptr(),
+                                            S.data_ptr(), O.data_ptr(), out.data_ptr(),
+                                            workspace.data_ptr(), stream.cuda_stream),
+           "gsample_gumbel_argmax_host")
+    if sync:
+        stream.synchronize()
     return out
 
 

@@ -206,7 +206,10 @@ void plan_sample(const DeviceInfo& d, const void* logits, gsample_dtype dtype, i
   p->units_per_row = (int32_t)nu;
   p->total_units = total;
   p->ctas = (int32_t)g;
-  p->warps = g * gsample::kWarps < total ? g * gsample::kWarps : total;
+  // A warp gets at least 8 units on the 128-bit path, so that its range still
+  // holds units after the split points move to 128-byte lines.
+  const int64_t max_warps = vec ? (total / 8 > 0 ? total / 8 : 1) : total;
+  p->warps = g * gsample::kWarps < max_warps ? g * gsample::kWarps : max_warps;
   *vec_out = vec;
 }
 
@@ -274,6 +277,27 @@ gsample_status run_sample(const void* logits, gsample_dtype dtype, int64_t B, in
     return GSAMPLE_ERR_CUDA;
   }
   return GSAMPLE_OK;
+}
+
+// The device address of a page-locked host buffer (cudaHostAlloc,
+// cudaMallocHost or cudaHostRegister) on the current device, or null when `p`
+// is not one.
+const void* mapped_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+bool is_device_memory(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice;
 }
 
 gsample_status run_categorical(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
@@ -424,6 +448,30 @@ gsample_status gsample_gumbel_argmax(const void* logits, gsample_dtype dtype, in
                                      gsample_stream_t stream) {
   if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
   return run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
+                    (cudaStream_t)stream);
+}
+
+gsample_status gsample_gumbel_argmax_host(const void* logits, gsample_dtype dtype, int64_t B,
+                                          int64_t V, int64_t ld, const float* temperature,
+                                          const uint64_t* seed, const uint64_t* offset,
+                                          int64_t* out_idx, void* workspace,
+                                          gsample_stream_t stream) {
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (st != GSAMPLE_OK || B == 0) return st;
+  if (!temperature || !seed || !offset) return GSAMPLE_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  const void* x = mapped_view(logits);
+  const void* t = mapped_view(temperature);
+  const void* s = mapped_view(seed);
+  const void* o = mapped_view(offset);
+  const void* out = mapped_view(out_idx);
+  if (!x || !t || !s || !o || !out) return GSAMPLE_ERR_INVALID_ARG;
+  if (!is_device_memory(workspace)) return GSAMPLE_ERR_WORKSPACE;
+  return run_sample(x, dtype, B, V, ld, static_cast<const float*>(t),
+                    static_cast<const uint64_t*>(s), static_cast<const uint64_t*>(o),
+                    static_cast<int64_t*>(const_cast<void*>(out)), workspace, 0,
                     (cudaStream_t)stream);
 }
 

@@ -647,6 +647,24 @@ __device__ __forceinline__ float score_of_hint(uint32_t h) {
   return h == 0u ? -INFINITY : score_of_key((unsigned long long)h << 32 | 1ull);
 }
 
+// Start of warp w's range of units (w = NW gives the end of the last). The
+// units are dealt in near-equal shares; on the 128-bit path each split point
+// then moves down, within its row, to a unit that starts a 128-byte line.
+// Host-resident logits (read over the CPU-GPU link) arrive in whole 128-byte
+// lines: with ranges that split lines, both neighbours fetch the shared line,
+// and host reads measured a third slower. Device reads are unaffected.
+template <bool VEC>
+__device__ __forceinline__ int64_t split_point(const SampleParams& p, int64_t w) {
+  const int64_t U = p.total_units, NW = p.warps;
+  const int64_t base = U / NW, rem = U % NW;
+  const int64_t u = w * base + (w < rem ? w : rem);
+  if (!VEC || u >= U) return u;
+  const int64_t NU = p.units_per_row, b = u / NU, l = u - b * NU;
+  const uint64_t row_unit = (uint64_t)(uintptr_t)(p.logits + b * p.ld_bytes) / 16u;
+  const int64_t la = l - (int64_t)((row_unit + (uint64_t)l) & 7u);
+  return b * NU + (la > 0 ? la : 0);
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kernel(const SampleParams p) {
   using C = Cfg<DT, VEC>;
@@ -660,9 +678,8 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
   const int64_t U = p.total_units, NU = p.units_per_row, NW = p.warps;
   const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
   if (gw >= NW) return;
-  const int64_t base = U / NW, rem = U % NW;
-  const int64_t u_begin = gw * base + (gw < rem ? gw : rem);
-  const int64_t u_end = u_begin + base + (gw < rem ? 1 : 0);
+  const int64_t u_begin = split_point<VEC>(p, gw), u_end = split_point<VEC>(p, gw + 1);
+  if (u_begin >= u_end) return;  // no units (only with fewer than 8 units per warp)
 
   // Prologue: the first kStages - 1 tiles go in flight.
   TileCursor cur = segment_at(u_begin / NU, u_begin, u_end, NU, C::kTile);
