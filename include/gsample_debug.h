@@ -28,6 +28,20 @@ gsample_status gsample_debug_philox(uint64_t seed, uint32_t row, uint64_t offset
 gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gumbel,
                                     float* bound, gsample_stream_t stream);
 
+/* The two word tests of the sampled path's exact pruning, for a row whose best
+ * known score is L at temperature T > 0 ("Softmax-free GPU sampling",
+ * Background: an element can win only if x/T + g reaches L, and g is at most
+ * -log(1 - u)). For each j:
+ *   flags[j] bit 0: the element test, 1 - u(words[j]) <= 2^((x[j]/T - lm)*log2 e)
+ *                   (x[j] >= the logit threshold when L is not finite);
+ *   flags[j] bit 1: the group test the kernels run first, words[j] >= threshold[j];
+ *   threshold[j]:   the integer word threshold computed from x[j] alone.
+ * The group test must pass wherever the element test does. x, words: device
+ * arrays of n entries; threshold (uint32) and flags (uint8): device outputs. */
+gsample_status gsample_debug_word_test(const float* x, const uint32_t* words, int64_t n, float L,
+                                       float T, uint32_t* threshold, uint8_t* flags,
+                                       gsample_stream_t stream);
+
 /* gsample_gumbel_argmax / gsample_hlg_gumbel_argmax with an explicit number
  * of CTAs (0 = the library's choice). ctas is clamped to [1, number of 16-byte
  * units in the batch]. hlg == NULL selects the plain sampler; a positive ctas

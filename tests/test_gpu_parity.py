@@ -148,6 +148,31 @@ def test_special_values():
         Tally().add(got, ref, gap, greedy_mask=np.full(B, T <= 0), where="T=%g" % T)
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("path", ["flat", "cluster"])
+def test_nan_runs_beside_live_groups(dtype, path):
+    """Runs of NaN logits covering whole 4-element groups, in the same tiles as
+    logits within reach of the row's best (the dense path's word test lets
+    such groups through to the exact pass, which must reject them), at T = 1
+    and at a high temperature where many groups pass."""
+    B, V = 6, 40000
+    rng = np.random.default_rng([dtype, len(path)])
+    x = (rng.standard_normal((B, V)) * 2).astype(np.float32)
+    for r in range(B):
+        starts = rng.integers(0, V // 8, 200) * 8
+        for s0 in starts:
+            x[r, s0:s0 + 8 * (1 + r % 3)] = np.nan
+    x[0, : V // 2] = np.nan
+    x = W.roundtrip(x, dtype)
+    for T in (1.0, 50.0):
+        b = W.Batch("nanruns", W.encode(x, dtype), dtype, np.full(B, T, np.float32),
+                    W.splitmix64(5, B), np.full(B, 11, np.uint64))
+        got = gpu_gumbel(b, ctas=64) if path == "flat" else gpu_gumbel(b, cluster=8)
+        ref, gap = _oracle_rows(b)
+        assert not np.isnan(x[np.arange(B), got]).any()
+        Tally().add(got, ref, gap, where="%s T=%g" % (path, T))
+
+
 def test_temperature_edge_values_route_to_greedy():
     B, V = 6, 4096
     b = _small(B, V, W.F32, seed=4, T=np.array([0.0, -1.0, np.nan, -0.0, 1e-30, 3.0], np.float32))

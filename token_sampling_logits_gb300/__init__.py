@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
             "gsample_status_string": (ctypes.c_char_p, [_int]),
             "gsample_debug_philox": (_int, [_u64, _u32, _u64, _i64, _i64, _vp, _vp]),
             "gsample_debug_gumbel": (_int, [_vp, _i64, _vp, _vp, _vp]),
+            "gsample_debug_word_test": (_int, [_vp, _vp, _i64, ctypes.c_float, ctypes.c_float, _vp,
+                                               _vp, _vp]),
             "gsample_debug_sample_ex": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                                _vp, _vp, _i32, _vp]),
             "gsample_debug_planned_ctas": (_i32, [_int, _i64, _i64, _i64, _vp, _i32]),

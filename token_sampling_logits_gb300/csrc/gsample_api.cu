@@ -544,6 +544,23 @@ gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gum
   return GSAMPLE_OK;
 }
 
+gsample_status gsample_debug_word_test(const float* x, const uint32_t* words, int64_t n, float L,
+                                       float T, uint32_t* threshold, uint8_t* flags,
+                                       gsample_stream_t stream) {
+  if (n < 0 || !(T > 0.0f)) return GSAMPLE_ERR_INVALID_ARG;
+  if (n == 0) return GSAMPLE_OK;
+  if (!x || !words || !threshold || !flags) return GSAMPLE_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  const gsample_status st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  if (gsample::launch_debug_word_test(x, words, n, L, T, threshold, flags, (cudaStream_t)stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
 gsample_status gsample_debug_sample_ex(const void* logits, gsample_dtype dtype, int64_t B,
                                        int64_t V, int64_t ld, const float* temperature,
                                        const uint64_t* seed, const uint64_t* offset,

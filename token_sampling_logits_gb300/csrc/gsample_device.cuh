@@ -301,12 +301,31 @@ __device__ __forceinline__ void score_group(uint32_t gid, float x0, float x1, fl
   *bi_io = bi;
 }
 
-// Can the group still reach L, given its largest logit and largest Philox word
-// (v = 1 - u only shrinks as the word grows, so one test covers all four)?
-__device__ __forceinline__ bool group_may_reach(float xm, const uint4& w, const Prune& pr,
-                                                const ReachTest& rt) {
-  if (!pr.use_bound) return xm >= pr.thr_x;
-  return may_reach(xm, max(max(w.x, w.y), max(w.z, w.w)), rt);
+// The group test as an integer threshold on the group's largest Philox word,
+// computed from its largest logit alone, before the block is known (v = 1 - u
+// only shrinks as the word grows, so one word covers all four elements).
+// may_reach(x, w) is v = (2k+1)*2^-24 <= e with k = 2^23 - 1 - (w >> 9) and
+// e = 2^(x*a + c). That holds iff w >= ceil(2^23 - 0.5 - e*2^23) * 512, and
+// that threshold is at least 2^32 - 256 - e*2^32. The fma below rounds once,
+// by at most 128 at these magnitudes, so truncating 2^32 - 1024 - e*2^32
+// (saturated to [0, 2^32 - 1]) never exceeds the exact threshold: every word
+// that passes may_reach passes this test, and only words within about 1200 of
+// the boundary pass this one alone. The exact pass tests every element again.
+// +inf logits give threshold 0 (always pass). So does a NaN group maximum,
+// which needs all four logits NaN: such a group then goes through the exact
+// pass, which rejects it. Only the dense path meets one: the compacted and
+// cluster paths take groups with xm >= thr_x, and a tile whose groups are all
+// NaN fails the tile test. Without a finite L the test is x >= thr_x.
+__device__ __forceinline__ uint32_t word_threshold(float xm, const Prune& pr, const ReachTest& rt) {
+  const float e = pr.use_bound ? ex2_approx(fmaf(xm, rt.a, rt.c))
+                               : (xm >= pr.thr_x ? INFINITY : 0.0f);
+  uint32_t w;
+  asm("cvt.rzi.sat.u32.f32 %0, %1;" : "=r"(w) : "f"(fmaf(-e, 4294967296.0f, 4294966272.0f)));
+  return w;
+}
+
+__device__ __forceinline__ uint32_t max_word(const uint4& w) {
+  return max(max(w.x, w.y), max(w.z, w.w));
 }
 
 // ---------------------------------------------------------------------------

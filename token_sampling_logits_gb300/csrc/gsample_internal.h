@@ -106,6 +106,8 @@ cudaError_t launch_categorical(const RowClusterParams& p, int dtype, bool vec, c
 
 cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
                                 int64_t n, uint32_t* out, cudaStream_t stream);
+cudaError_t launch_debug_word_test(const float* x, const uint32_t* w, int64_t n, float L, float T,
+                                   uint32_t* threshold, uint8_t* flags, cudaStream_t stream);
 cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, float* bound,
                                 cudaStream_t stream);
 

@@ -423,23 +423,21 @@ __device__ __forceinline__ void compact_batch(uint32_t stage, const unsigned sho
                                               unsigned char* rbase, int& rcnt, float& bs,
                                               int32_t& bi) {
   const int lane = threadIdx.x & 31;
-  uint32_t q[N], g[N];
-  float xm[N];
+  uint32_t q[N], g[N], wt[N];
   bool valid[N];
 #pragma unroll
   for (int j = 0; j < N; ++j) {
     const int idx = base + lane + 32 * j;
     valid[j] = idx < cnt;
     q[j] = valid[j] ? (uint32_t)clist[idx] : 0u;
-    xm[j] = group_max_at<DT, VEC>(stage, q[j]);
+    wt[j] = word_threshold(group_max_at<DT, VEC>(stage, q[j]), pr, rt);
     g[j] = g0 + q[j];
   }
   uint4 w[N];
   philox_row_xn<N>(g, rc.ph, w);
   uint32_t need = 0;
 #pragma unroll
-  for (int j = 0; j < N; ++j)
-    need |= (valid[j] && group_may_reach(xm[j], w[j], pr, rt)) ? (1u << j) : 0u;
+  for (int j = 0; j < N; ++j) need |= (valid[j] && max_word(w[j]) >= wt[j]) ? (1u << j) : 0u;
   append_rare<DT, VEC, N>(need, q, stage, g0, rc, pr, rbase, rcnt, bs, bi);
 }
 
@@ -493,6 +491,11 @@ __device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const 
   for (int i = 0; i < 4; ++i) c4 += xm[i] >= pr.thr_x ? 1 : 0;
   const int sample = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)c4);
   if (sample * GSAMPLE_DENSE_DEN > 128 * GSAMPLE_DENSE_NUM) {
+    // Every group's word threshold first: it needs only the logits, so its
+    // exponential runs ahead of, not after, the Philox chains.
+    uint32_t wt[NG];
+#pragma unroll
+    for (int i = 0; i < NG; ++i) wt[i] = word_threshold(xm[i], pr, rt);
     uint32_t need = 0;
     const uint32_t gl = g0 + lane_group<DT, VEC>(0, lane);
 #pragma unroll
@@ -504,8 +507,7 @@ __device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const 
       uint4 w[4];
       philox_row_x4(g, rc.ph, w);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        need |= group_may_reach(xm[b + j], w[j], pr, rt) ? (1u << (b + j)) : 0u;
+      for (int j = 0; j < 4; ++j) need |= max_word(w[j]) >= wt[b + j] ? (1u << (b + j)) : 0u;
     }
     append_rare<DT, VEC, 0>(need, nullptr, stage, g0, rc, pr, rbase, rcnt, bs, bi);
     return;
@@ -863,6 +865,21 @@ __global__ void debug_gumbel_kernel(const uint32_t* words, int64_t n, float* g, 
   }
 }
 
+// flags[j]: bit 0 = the element test may_reach(x[j], w[j]), bit 1 = the
+// group test w[j] >= word_threshold(x[j]); threshold[j] = that threshold.
+__global__ void debug_word_test_kernel(const float* x, const uint32_t* w, int64_t n, float L,
+                                       float T, uint32_t* threshold, uint8_t* flags) {
+  const Prune pr = make_prune(L, T);
+  const ReachTest rt = make_reach(pr, 1.0f / T);
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+       j += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t t = word_threshold(x[j], pr, rt);
+    const bool elem = pr.use_bound ? may_reach(x[j], w[j], rt) : (x[j] >= pr.thr_x);
+    threshold[j] = t;
+    flags[j] = (uint8_t)((elem ? 1 : 0) | (w[j] >= t ? 2 : 0));
+  }
+}
+
 unsigned grid_for(int64_t n) {
   const int64_t blocks = (n + 255) / 256;
   return (unsigned)(blocks < 4096 ? (blocks < 1 ? 1 : blocks) : 4096);
@@ -879,6 +896,12 @@ cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, in
 cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, float* bound,
                                 cudaStream_t stream) {
   debug_gumbel_kernel<<<grid_for(n), 256, 0, stream>>>(words, n, g, bound);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_word_test(const float* x, const uint32_t* w, int64_t n, float L, float T,
+                                   uint32_t* threshold, uint8_t* flags, cudaStream_t stream) {
+  debug_word_test_kernel<<<grid_for(n), 256, 0, stream>>>(x, w, n, L, T, threshold, flags);
   return cudaGetLastError();
 }
 

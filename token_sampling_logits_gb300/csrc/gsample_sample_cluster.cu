@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
     for (int32_t it = 0; it < n_iter; it += kUPB) {
       uint4 r[kUPB];
       float xm[4];
-      uint32_t g[4];
+      uint32_t g[4], wt[4];
       bool ok[4];
 #pragma unroll
       for (int j = 0; j < kUPB; ++j) {
@@ -142,11 +142,13 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
         }
       }
       if (!__any_sync(0xFFFFFFFFu, ok[0] || ok[1] || ok[2] || ok[3])) continue;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) wt[jj] = word_threshold(xm[jj], pr, rt);
       uint4 w[4];
       philox_row_x4(g, ph, w);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        if (ok[jj] && group_may_reach(xm[jj], w[jj], pr, rt)) {
+        if (ok[jj] && max_word(w[jj]) >= wt[jj]) {
           const uint4 rj = r[jj / C::kGPU];
           const int h = jj % C::kGPU;
           score_group(g[jj], elt<DT, VEC>(rj, 4 * h), elt<DT, VEC>(rj, 4 * h + 1),
