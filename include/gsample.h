@@ -32,7 +32,13 @@
  *     Two launches that are in flight at the same time (different streams) must
  *     not share a workspace.
  *   - stream: a cudaStream_t (NULL = legacy default stream). Calls only enqueue
- *     work on it and never synchronise; GSAMPLE_OK means "launched".
+ *     work on it and never synchronise; GSAMPLE_OK means "launched". Kernels are
+ *     launched with programmatic stream serialization: each may be scheduled
+ *     while the previous kernel of the stream drains, waits for it to complete
+ *     before touching memory, and lets the next kernel be scheduled early. A
+ *     kernel that follows on the stream with that launch attribute must wait
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before reading the
+ *     indices; one launched without it sees the usual stream order.
  *   - The caller owns every buffer; the library allocates nothing and keeps no
  *     global state apart from cached device attributes.
  *   - Errors: arguments are checked on the host before anything is launched and

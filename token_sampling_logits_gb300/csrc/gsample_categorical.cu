@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kCatThreads) categorical_kernel(const RowClust
   __shared__ float s_row[3];  // M, target CTA's local target, flags
   __shared__ int32_t s_pick[2];
 
+  pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -385,13 +386,14 @@ cudaError_t launch_categorical(const RowClusterParams& p, int dtype, bool vec, c
   cfg.blockDim = dim3(kCatThreads);
   cfg.dynamicSmemBytes = resident ? need : 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   void* args[] = {const_cast<RowClusterParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }

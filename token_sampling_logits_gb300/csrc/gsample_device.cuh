@@ -30,6 +30,18 @@ struct WsRow {
 };
 static_assert(sizeof(WsRow) == 16, "workspace row is 16 bytes");
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization, so its CTAs may be scheduled while the
+// previous kernel of the stream drains. Each kernel first waits for that
+// kernel to complete and its memory to be visible (griddepcontrol.wait),
+// before touching global memory, then lets the next kernel of the stream be
+// scheduled early in turn. A kernel that follows on the same stream with the
+// same launch attribute must likewise wait before reading the indices.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al. 2011): two 32x32->64 multiplies per round with
 // the paper's 4x32 multipliers, a Weyl-sequence key schedule (golden ratio and

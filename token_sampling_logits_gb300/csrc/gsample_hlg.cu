@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   __shared__ int s_pinf;
   __shared__ RowState s_row;
 
+  pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -462,13 +463,14 @@ cudaError_t launch_hlg(const HlgParams& p, int dtype, bool vec, cudaStream_t str
   cfg.blockDim = dim3(kHlgThreads);
   cfg.dynamicSmemBytes = resident ? need : 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   void* args[] = {const_cast<HlgParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }

@@ -10,6 +10,15 @@
 
 namespace gsample {
 
+// The launch attribute that pairs with pdl_wait_then_release() in every kernel.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+
 // One launch of the row sampler. Rows are cut into 16-byte units (or 4-element
 // units when a row does not start on a 16-byte boundary); the B * units_per_row
 // units are split into `ctas` near-equal contiguous ranges, one per CTA.

@@ -671,6 +671,7 @@ template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kernel(const SampleParams p) {
   using C = Cfg<DT, VEC>;
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait_then_release();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   unsigned char* wbase = smem + (size_t)warp * C::kWarpBytes;
@@ -836,8 +837,15 @@ int sample_ctas_per_sm(int dtype, bool vec) {
 cudaError_t launch_sample(const SampleParams& p, int dtype, bool vec, cudaStream_t stream) {
   void* fn = select_kernel(dtype, vec);
   void* args[] = {const_cast<SampleParams*>(&p)};
-  return cudaLaunchKernel(fn, dim3((unsigned)p.ctas), dim3(kThreads), args,
-                          sample_smem_bytes(dtype, vec), stream);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sample_smem_bytes(dtype, vec);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // ---------------------------------------------------------------------------

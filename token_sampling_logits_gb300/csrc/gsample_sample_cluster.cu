@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
   __shared__ unsigned long long s_red[kRcWarps];
   __shared__ unsigned long long s_best;  // this CTA's best key, read by rank 0
 
+  pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -241,13 +242,14 @@ cudaError_t launch_sample_cluster(const RowClusterParams& p, int dtype, bool vec
   cfg.blockDim = dim3(kRcThreads);
   cfg.dynamicSmemBytes = resident ? need : 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   void* args[] = {const_cast<RowClusterParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
