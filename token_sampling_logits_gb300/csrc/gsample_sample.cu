@@ -334,19 +334,35 @@ __device__ __forceinline__ void raw_values(const RareRaw<DT, VEC>& r, float x[4]
 }
 
 // Score the listed groups exactly (one per lane) against the current bound.
+// Out of line: it runs once per 32 listed groups, and keeping its logarithms
+// out of the tile loop keeps that loop's code small.
+struct Best {
+  float s;
+  int32_t i;
+};
+
 template <int DT, bool VEC>
-__device__ __forceinline__ void flush_rare(const unsigned char* rbase, int rcnt, const RowCtx& rc,
-                                           const Prune& pr, float& bs, int32_t& bi) {
+__device__ __noinline__ Best flush_rare_cold(const unsigned char* rbase, int rcnt, float T, float rT,
+                                             PhiloxRow ph, Prune pr, float bs, int32_t bi) {
   const int lane = threadIdx.x & 31;
   __syncwarp();  // the entries of every lane are visible
   if (lane < rcnt) {
     const uint32_t g = reinterpret_cast<const uint32_t*>(rbase)[lane];
     float x[4];
     raw_values<DT, VEC>(reinterpret_cast<const RareRaw<DT, VEC>*>(rbase + kRareRawOff)[lane], x);
-    const uint4 w = philox_row_1(g, rc.ph);
-    score_group(g, x[0], x[1], x[2], x[3], w, pr, make_reach(pr, rc.rT), rc.T, &bs, &bi);
+    const uint4 w = philox_row_1(g, ph);
+    score_group(g, x[0], x[1], x[2], x[3], w, pr, make_reach(pr, rT), T, &bs, &bi);
   }
   __syncwarp();  // every lane has read its entry before the list is refilled
+  return Best{bs, bi};
+}
+
+template <int DT, bool VEC>
+__device__ __forceinline__ void flush_rare(const unsigned char* rbase, int rcnt, const RowCtx& rc,
+                                           const Prune& pr, float& bs, int32_t& bi) {
+  const Best r = flush_rare_cold<DT, VEC>(rbase, rcnt, rc.T, rc.rT, rc.ph, pr, bs, bi);
+  bs = r.s;
+  bi = r.i;
 }
 
 // Tile-local group q of this lane's i-th group (unit i / kGPU, half i % kGPU).
