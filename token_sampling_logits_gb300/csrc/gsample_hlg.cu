@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   __shared__ Moments s_part;            // this CTA's partial, read by the whole cluster
   __shared__ unsigned long long s_red[kHlgWarps];
   __shared__ unsigned long long s_best;  // this CTA's best key, read by rank 0
+  __shared__ unsigned long long s_lbest;  // this CTA's best first candidate, read by the cluster
+  __shared__ unsigned long long s_lrow;   // the row's best first candidate
   __shared__ int s_pinf;
   __shared__ RowState s_row;
 
@@ -304,7 +306,19 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
       const uint4 blk = philox_row_1((uint32_t)cand_i >> 2, ph);
       take_better(hlg_score(cv, rs, cand_x, word_of(blk, cand_i & 3), rT), cand_i, bs, bi);
     }
-    const float L = score_of_key(block_best(bs, bi, s_red));
+    // The bound: the best first candidate of the whole row, over the cluster.
+    {
+      const unsigned long long kc = block_best(bs, bi, s_red);
+      if (threadIdx.x == 0) s_lbest = kc;
+    }
+    cluster.sync();
+    if (warp == 0) {
+      unsigned long long k = lane < p.cluster ? *cluster.map_shared_rank(&s_lbest, lane) : 0ull;
+      k = warp_max_u64(k);
+      if (lane == 0) s_lrow = k;
+    }
+    __syncthreads();
+    const float L = score_of_key(s_lrow);
 
     // Exact pruning in logit space: x < x_thr implies tone(x + shift)/T + max g < L.
     float x_thr = -INFINITY;
