@@ -6,8 +6,8 @@
 //
 // Work split. The B rows are cut into 16-byte units. All B * units_per_row
 // units are dealt to the warps of one wave of CTAs, in near-equal contiguous
-// ranges. Each warp walks its range in tiles of 32 lanes x kVPT units; a tile
-// never crosses a row. Warps never wait for one another: there is no CTA-wide
+// ranges whose ends sit on 128-byte lines of the row. Each warp walks its range
+// in tiles of 32 lanes x kVPT units; a tile never crosses a row. Warps never wait for one another: there is no CTA-wide
 // barrier in the kernel.
 //
 // Memory pipeline. Each warp streams its tiles through a ring of kStages tiles
@@ -26,10 +26,11 @@
 // element with x/T + max(g) < L cannot win, so Philox and the logarithms are
 // skipped for it: a tile whose logits all sit below L - max(g) is skipped
 // whole. In the other tiles every 4-element group gets its Philox block, four
-// independent blocks per lane at a time, and a cheap bound on g from the
-// largest word of the block rejects almost every group before the two exact
+// independent blocks per lane at a time, and a bound on g from the largest
+// word of the block (an integer threshold computed from the group's logits
+// before the block) rejects almost every group before the two exact
 // logarithms. The few survivors wait in a per-warp list and are scored 32 at a
-// time, one per lane. Where only a small share of a tile's groups reaches the
+// time, one per lane, out of line. Where only a small share of a tile's groups reaches the
 // logit threshold, those groups are compacted first and only they get Philox.
 #include <cstdint>
 #include <type_traits>
