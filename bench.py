@@ -245,6 +245,27 @@ def make_pool():
     return ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")), cores
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm implementer
+    and part numbers), for the CPU-baseline record."""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+        if fields.get("model name"):
+            return fields["model name"]
+        if fields.get("CPU implementer"):
+            return "Arm implementer %s part %s" % (fields["CPU implementer"],
+                                                  fields.get("CPU part", "?"))
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 def oracle_rows_per_sec(pool, batch: W.Batch, rows, step: int) -> float:
     jobs = [(np.ascontiguousarray(batch.logits[r]), batch.dtype, float(batch.temperature[r]),
              int(batch.seed[r]), int(r), step) for r in rows]
@@ -353,6 +374,23 @@ class Runner:
         if rem:
             self.graph(rem).replay()
         self.launches += steps
+
+    def single_launch_us(self, n: int = 25) -> float:
+        """Median of n single launches, each un-captured and bracketed by its own
+        pair of CUDA events with the stream idle before it (launch latency
+        included, unlike the graph-replayed µs/step)."""
+        torch = self.torch
+        times = []
+        for k in range(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            self._launch_range(1, k)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1000.0)
+        return statistics.median(times)
 
     def prepare(self, steps: int):
         full, rem = divmod(steps, self.ring)
@@ -481,7 +519,8 @@ def e2e_steps(batch: W.Batch, steps: int, dist: Dist, l2: int):
 
 
 def extra_table(dist: Dist, l2: int):
-    """µs/step of the other workloads (graph-replayed, rotating pools)."""
+    """µs/step of the other workloads (graph-replayed, rotating pools), and the
+    latency of one un-captured launch of each."""
     import token_sampling_logits_gb300 as gs
 
     rows = []
@@ -492,20 +531,22 @@ def extra_table(dist: Dist, l2: int):
                       pivot_offset=p["c"])
     cases.append(("hlg", W.hlg(), hp))
     cases.append(("mixed_greedy", W.mixed_greedy(), None))
-    def timed(b, h=None, categorical=False):
+    def timed(b, h=None, categorical=False, single=False):
         r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500, categorical=categorical)
         steps = r.ring * max(1, (2000 if b.B * b.V < 50_000_000 else 500) // r.ring)
         ms, _ = time_steps(r, steps, 50, dist)
+        one = r.single_launch_us() if single else None
         del r
-        return ms * 1000 / steps
+        return (ms * 1000 / steps, one) if single else ms * 1000 / steps
 
     for kind, b, h in cases:
-        us = timed(b, h)
+        us, one = timed(b, h, single=True)
         nbytes = b.B * (b.V * (4 if b.dtype == W.F32 else 2) + PER_ROW_PARAM_BYTES)
         row = {"workload": kind, "B": b.B, "V": b.V, "dtype": W.DTYPE_NAMES[b.dtype],
                "us_per_step": round(us, 3), "rows_per_s": round(b.B / us * 1e6, 1),
                "GBps": round(nbytes / us / 1e3, 1),
-               "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4)}
+               "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4),
+               "single_launch_us": round(one, 3)}
         if kind == "sweep":
             # The issue's comparison: the categorical (softmax + inverse-CDF)
             # path against Gumbel-max on the same V x B grid.
@@ -567,7 +608,7 @@ def run_ours(args, dist: Dist):
         for step in range(4):
             rps.append(oracle_rows_per_sec(pool, batch, sample_rows, step))
         cpu = {"value": round(statistics.median(rps), 2), "unit": "rows/s", "cores": cores,
-               "kind": "oracle",
+               "cpu": cpu_model(), "kind": "oracle",
                "sample": "%d rows x 4 decode steps of the headline batch (bf16, V=%d), one row "
                          "per task over a spawn pool" % (batch.B, batch.V)}
         pool.shutdown()
@@ -688,7 +729,7 @@ def run_reference(args, dist: Dist):
                                "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
                    "global_batch": batch.B, "vocab": batch.V, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "cpu": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

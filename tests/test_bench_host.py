@@ -109,3 +109,9 @@ def test_side_workload_needs_quick(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--categorical"])
     with pytest.raises(SystemExit):
         b.parse_args()
+
+
+def test_cpu_model_names_the_host():
+    b = _bench()
+    name = b.cpu_model()
+    assert isinstance(name, str) and name
