@@ -377,18 +377,38 @@ class Runner:
 
     def single_launch_us(self, n: int = 25) -> float:
         """Median of n single launches, each un-captured and bracketed by its own
-        pair of CUDA events with the stream idle before it (launch latency
-        included, unlike the graph-replayed µs/step)."""
+        pair of CUDA events with the stream idle before it. The span includes
+        the host side of the C call (argument checks and the launch itself),
+        unlike the graph-replayed µs/step."""
         torch = self.torch
+        st = torch.cuda.current_stream().cuda_stream
+        L = self.gs.lib()
+        B = self.B
         times = []
         for k in range(n):
+            x = self.pool[k % self.P]
+            out = self.out.data_ptr() + 8 * B * (k % self.ring)
+            offs = self.offs.data_ptr() + 8 * B * (k % self.ring)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             e0.record()
-            self._launch_range(1, k)
+            if self.categorical:
+                rc = L.gsample_categorical(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                           self.T.data_ptr(), self.S.data_ptr(), offs, out, st)
+            elif self.hp is None:
+                rc = L.gsample_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                             self.T.data_ptr(), self.S.data_ptr(), offs, out,
+                                             self.ws.data_ptr(), st)
+            else:
+                rc = L.gsample_hlg_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
+                                                 self.T.data_ptr(), self.S.data_ptr(), offs,
+                                                 self.ctypes.byref(self.hp), out,
+                                                 self.ws.data_ptr(), st)
             e1.record()
             torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError("sampler launch failed: " + self.gs.status_string(rc))
             times.append(e0.elapsed_time(e1) * 1000.0)
         return statistics.median(times)
 
