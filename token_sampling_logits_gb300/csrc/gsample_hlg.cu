@@ -148,6 +148,11 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   __shared__ unsigned long long s_lrow;   // the row's best first candidate
   __shared__ int s_pinf;
   __shared__ RowState s_row;
+  // Per warp: groups that passed the word test, waiting for an exact pass with
+  // one group per lane (row-local group index, its four logits, its words).
+  __shared__ uint32_t s_rg[kHlgWarps][32];
+  __shared__ float4 s_rx[kHlgWarps][32];
+  __shared__ uint4 s_rw[kHlgWarps][32];
 
   pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
@@ -344,6 +349,28 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
     // time (four units of binary32, two of 16-bit), one Philox block each.
     constexpr int kUPB = 4 / C::kGPU;  // units per batch
     const int32_t n_iter = (u_hi - u_lo + kHlgThreads - 1) / kHlgThreads;
+    // The warp's listed groups, scored exactly one per lane: the element's own
+    // word bound, then tone(z)/T + g.
+    int rcnt = 0;
+    auto flush = [&]() {
+      __syncwarp();
+      if (lane < rcnt) {
+        const uint32_t gg = s_rg[warp][lane];
+        const float4 xx = s_rx[warp][lane];
+        const uint4 ww = s_rw[warp][lane];
+        const float xs[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float x = xs[t];
+          if (!(x >= x_thr) || x == -INFINITY) continue;
+          if (word_test &&
+              !may_reach(tone_upper(cv, x + rs.shift), word_of(ww, t), ReachTest{wa, wc}))
+            continue;
+          take_better(hlg_score(cv, rs, x, word_of(ww, t), rT), (int32_t)(4 * gg + t), bs, bi);
+        }
+      }
+      __syncwarp();
+    };
     for (int32_t it = 0; it < n_iter; it += kUPB) {
       uint4 r[kUPB];
       float xm[4];
@@ -375,19 +402,26 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
           const uint32_t wm = max(max(w[jj].x, w[jj].y), max(w[jj].z, w[jj].w));
           need = may_reach(tone_upper(cv, xm[jj] + rs.shift), wm, ReachTest{wa, wc});
         }
-        if (need) {  // rare: the exact scores of the group's elements
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, need);
+        if (m == 0u) continue;
+        const int n = __popc(m);
+        if (rcnt + n > 32) {
+          flush();
+          rcnt = 0;
+        }
+        if (need) {
           const uint4 rj = r[jj / C::kGPU];
           const int h = jj % C::kGPU;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float x = elt<DT, VEC>(rj, 4 * h + t);
-            if (!(x >= x_thr) || x == -INFINITY) continue;
-            take_better(hlg_score(cv, rs, x, word_of(w[jj], t), rT), (int32_t)(4 * g[jj] + t),
-                        bs, bi);
-          }
+          const int pos = rcnt + __popc(m & ((1u << lane) - 1u));
+          s_rg[warp][pos] = g[jj];
+          s_rx[warp][pos] = make_float4(elt<DT, VEC>(rj, 4 * h), elt<DT, VEC>(rj, 4 * h + 1),
+                                        elt<DT, VEC>(rj, 4 * h + 2), elt<DT, VEC>(rj, 4 * h + 3));
+          s_rw[warp][pos] = w[jj];
         }
+        rcnt += n;
       }
     }
+    if (rcnt > 0) flush();
   }
 
   // The row's answer: each CTA's best key, merged by rank 0 over distributed
@@ -426,7 +460,7 @@ void* select_hlg(int dtype, bool vec, bool resident) {
   }
 }
 
-constexpr size_t kSmemLimit = 224 * 1024;  // leaves room for the static shared variables
+constexpr size_t kSmemLimit = 204 * 1024;  // leaves room for the static shared variables
 
 }  // namespace
 
