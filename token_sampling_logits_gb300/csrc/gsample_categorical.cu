@@ -81,6 +81,11 @@ __global__ void __launch_bounds__(kCatThreads) categorical_kernel(const RowClust
   const uint64_t pol = evict_first_policy();
   const float T = __ldg(p.temperature + b);
   const bool sampled = T > 0.0f;
+  // The row's seed and offset, requested now so that their latency hides
+  // behind the slice load.
+  const uint64_t sd = sampled ? __ldg(p.seed + b) : 0ull;
+  const uint64_t of = sampled ? __ldg(p.offset + b) : 0ull;
+  float u_row = 0.0f;
 
   if constexpr (RESIDENT) {
     for (int32_t u = u_lo + tid; u < u_hi; u += kCatThreads) {
@@ -90,7 +95,17 @@ __global__ void __launch_bounds__(kCatThreads) categorical_kernel(const RowClust
       else
         sts128(dst, load_unit<DT, VEC>(row, u, p.V, pol));
     }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  // The row's uniform (element 0's word of its Philox stream), needed only by
+  // warp 0 after the scans, is drawn while the slice is in flight.
+  if (warp == 0 && sampled) {
+    const uint4 blk = philox4x32_10(make_uint4(0u, (uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32)),
+                                    (uint32_t)sd, (uint32_t)(sd >> 32));
+    u_row = uniform_open(blk.x);
+  }
+  if constexpr (RESIDENT) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();  // each thread reads units other threads copied
   }
   auto unit_at = [&](int32_t u) -> uint4 {
@@ -249,10 +264,7 @@ __global__ void __launch_bounds__(kCatThreads) categorical_kernel(const RowClust
         if (lane >= o) inc += t;
       }
       const float S = __shfl_sync(0xFFFFFFFFu, inc, 31);
-      const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
-      const uint4 blk = philox4x32_10(make_uint4(0u, (uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32)),
-                                      (uint32_t)sd, (uint32_t)(sd >> 32));
-      const float t = uniform_open(blk.x) * S;
+      const float t = u_row * S;
       const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < p.cluster && t < inc);
       const unsigned pos = __ballot_sync(0xFFFFFFFFu, lane < p.cluster && tot > 0.0f);
       const int cstar = hit ? __ffs(hit) - 1 : 31 - __clz(pos);  // else: the last CTA with mass

@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   const uint64_t pol = evict_first_policy();
 
   const float T = __ldg(p.temperature + b);
+  // The row's seed and offset are requested now, so their latency hides behind
+  // the slice load.
+  const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
   // The row's curve: the launch's, or its own from the per-row array.
   HlgRowParams hp{p.m, p.w, p.beta_t, p.beta_h, p.pivot_offset, p.pivot_mode};
   if (p.rows) {
@@ -299,7 +302,6 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
 
     const Curve cv{hp.m, hp.w, hp.beta_t, hp.beta_h, 1.0f / hp.beta_t, 1.0f / hp.beta_h};
     const float rT = 1.0f / T;
-    const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
     const uint32_t k0 = (uint32_t)sd, k1 = (uint32_t)(sd >> 32);
     const uint32_t o0 = (uint32_t)of, o1 = (uint32_t)(of >> 32);
     const uint32_t row_id = (uint32_t)b;

@@ -63,6 +63,10 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
   const uint64_t pol = evict_first_policy();
   const float T = p.temperature ? __ldg(p.temperature + b) : 0.0f;
   const bool sampled = T > 0.0f;  // NaN and T <= 0: greedy
+  // The row's seed and offset are requested now, so their latency hides behind
+  // the slice load (greedy launches pass no arrays).
+  const uint64_t sd = p.seed ? __ldg(p.seed + b) : 0ull;
+  const uint64_t of = p.offset ? __ldg(p.offset + b) : 0ull;
 
   // Every unit of the thread's share is requested at once; the thread then
   // reads back its own units only, so its own wait is enough.
@@ -105,7 +109,6 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
     bs = cand_x;
     bi = cand_x > -INFINITY ? cand_i : INT32_MAX;
   } else {
-    const uint64_t sd = __ldg(p.seed + b), of = __ldg(p.offset + b);
     const PhiloxRow ph = philox_row((uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32), (uint32_t)sd,
                                     (uint32_t)(sd >> 32));
     if (cand_i != INT32_MAX && cand_x > -INFINITY) {
