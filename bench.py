@@ -201,13 +201,18 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def kernel_source_hash() -> str:
+# The sources that define the headline kernel (sample_kernel) and its launch
+# shape: the kernel, the device header it includes, and the planner.
+SAMPLE_KERNEL_SOURCES = ("gsample_api.cu", "gsample_device.cuh", "gsample_internal.h",
+                         "gsample_sample.cu")
+
+
+def kernel_source_hash(names=SAMPLE_KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_sampling_logits_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

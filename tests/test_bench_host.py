@@ -115,3 +115,20 @@ def test_cpu_model_names_the_host():
     b = _bench()
     name = b.cpu_model()
     assert isinstance(name, str) and name
+
+
+def test_kernel_source_hash_covers_the_headline_kernel_only(tmp_path, monkeypatch):
+    import shutil
+
+    b = _bench()
+    csrc = os.path.join(ROOT, "token_sampling_logits_gb300", "csrc")
+    copy = tmp_path / "token_sampling_logits_gb300" / "csrc"
+    shutil.copytree(csrc, copy)
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    h = b.kernel_source_hash()
+    with open(copy / "gsample_hlg.cu", "a") as f:
+        f.write("\n// another kernel's change\n")
+    assert b.kernel_source_hash() == h
+    with open(copy / "gsample_sample.cu", "a") as f:
+        f.write("\n// the headline kernel's change\n")
+    assert b.kernel_source_hash() != h
