@@ -157,3 +157,12 @@ def test_host_buffer_entry_validation():
     if not torch.cuda.is_available():
         # the pointer checks need the device: without one the call fails loudly
         assert call() == gs.ERR_CUDA
+
+
+def test_host_buffer_binding_rejects_pageable_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((2, 64), dtype=torch.float32)  # pageable host memory
+    with pytest.raises(ValueError):
+        gs.gumbel_argmax_host(x, 1.0, 0, 0)
+    with pytest.raises(ValueError):
+        gs.gumbel_argmax_host(torch.zeros(64), 1.0, 0, 0)  # not 2-D (and not pinned)
