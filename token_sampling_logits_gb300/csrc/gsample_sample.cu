@@ -530,14 +530,24 @@ __device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const 
     return;
   }
 
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int cnt = 0;
+  // The survivors' tile-local indices, lane by lane: each lane's mask, an
+  // exclusive scan of the lanes' counts, then each lane writes its own.
+  uint32_t keep = 0;
 #pragma unroll
-  for (int i = 0; i < NG; ++i) {
-    const bool keep = xm[i] >= pr.thr_x;
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-    if (keep) clist[cnt + __popc(m & lt_mask)] = (unsigned short)lane_group<DT, VEC>(i, lane);
-    cnt += __popc(m);
+  for (int i = 0; i < NG; ++i) keep |= xm[i] >= pr.thr_x ? (1u << i) : 0u;
+  const int mine = __popc(keep);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int cnt = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  int pos = incl - mine;
+  while (keep != 0u) {
+    const int i = __ffs(keep) - 1;
+    keep &= keep - 1u;
+    clist[pos++] = (unsigned short)lane_group<DT, VEC>(i, lane);
   }
   __syncwarp();
   for (int base = 0; base < cnt; base += 128) {
