@@ -166,3 +166,17 @@ def test_host_buffer_binding_rejects_pageable_tensors():
         gs.gumbel_argmax_host(x, 1.0, 0, 0)
     with pytest.raises(ValueError):
         gs.gumbel_argmax_host(torch.zeros(64), 1.0, 0, 0)  # not 2-D (and not pinned)
+
+
+def test_word_test_debug_entry_validation():
+    L = gs.lib()
+
+    def call(n=4, x=FAKE, w=FAKE, T=1.0, thr=FAKE, flags=FAKE):
+        return L.gsample_debug_word_test(x, w, n, 10.0, T, thr, flags, None)
+
+    assert call(n=0) == gs.OK                      # nothing to do
+    assert call(n=-1) == gs.ERR_INVALID_ARG
+    assert call(T=0.0) == gs.ERR_INVALID_ARG       # the test is defined for T > 0
+    assert call(T=float("nan")) == gs.ERR_INVALID_ARG
+    assert call(x=None) == gs.ERR_INVALID_ARG
+    assert call(flags=None) == gs.ERR_INVALID_ARG
