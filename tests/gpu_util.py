@@ -10,6 +10,12 @@ import token_sampling_logits_gb300 as gs
 import workloads as W
 
 NEAR_TIE = 1e-5
+# The parity rule's bound on the share of exempted (near-tie) rows, per config.
+MAX_NEAR_FRACTION = 1e-4
+# Rows checked per config over the whole session (name -> Tally); printed as a
+# table at the end of the run (tests/conftest.py) and written as JSON to the
+# path in GSAMPLE_PARITY_TABLE if that variable is set.
+PARITY = {}
 
 
 def torch_mod():
@@ -77,6 +83,54 @@ class Tally:
         self.near += int(near.sum())
         self.near_mismatch += int(((gpu != ref) & near).sum())
 
+    def merge(self, other: "Tally"):
+        self.rows += other.rows
+        self.near += other.near
+        self.near_mismatch += other.near_mismatch
+        return self
+
     @property
     def near_fraction(self):
         return self.near / max(1, self.rows)
+
+    def summary(self):
+        return "rows %d, near-tie rows %d (fraction %.2e), near-tie mismatches %d" % (
+            self.rows, self.near, self.near_fraction, self.near_mismatch)
+
+
+def register(config: str, tally: Tally, assert_bound: bool = True):
+    """Add a test's rows to its config's session total. With assert_bound, the
+    test's own rows must already meet the near-tie bound; the workload tests
+    check at least 2e4 rows each, so that one exempted row stays within it."""
+    PARITY.setdefault(config, Tally()).merge(tally)
+    print("%s: %s" % (config, tally.summary()))
+    if assert_bound:
+        assert tally.rows >= int(2 / MAX_NEAR_FRACTION), (config, tally.rows)
+        assert tally.near_fraction < MAX_NEAR_FRACTION, (config, tally.summary())
+
+
+def gpu_gumbel_steps(batch: W.Batch, steps, logits_dev=None):
+    """The CUDA path at every decode step in `steps` (offset = step for every
+    row): int64[len(steps), B]."""
+    torch = torch_mod()
+    x = logits_dev if logits_dev is not None else to_device(batch.logits, batch.dtype)
+    T, S, _ = rows_to_device(batch)
+    outs = []
+    for s in steps:
+        O = torch.full((batch.B,), int(s), dtype=torch.int64, device=x.device)
+        outs.append(gs.gumbel_argmax(x, T, S, O))
+    torch.cuda.synchronize()
+    return torch.stack(outs).cpu().numpy()
+
+
+def gpu_hlg_steps(batch: W.Batch, params, steps, logits_dev=None):
+    """The HLG kernel at every decode step in `steps`: int64[len(steps), B]."""
+    torch = torch_mod()
+    x = logits_dev if logits_dev is not None else to_device(batch.logits, batch.dtype)
+    T, S, _ = rows_to_device(batch)
+    outs = []
+    for s in steps:
+        O = torch.full((batch.B,), int(s), dtype=torch.int64, device=x.device)
+        outs.append(gs.hlg_gumbel_argmax(x, T, S, O, params))
+    torch.cuda.synchronize()
+    return torch.stack(outs).cpu().numpy()

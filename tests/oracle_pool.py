@@ -79,3 +79,19 @@ def hlg_row_steps(row, dtype, T, seed, row_id, base: int, steps: int, extra: dic
     jobs = [(np.ascontiguousarray(row), dtype, T, seed, row_id, base + int(a), int(b - a), extra)
             for a, b in zip(edges[:-1], edges[1:]) if b > a]
     return np.concatenate(list(pool().map(_hlg_steps_job, jobs)))
+
+
+def rows_at_steps(kind: str, logits, dtype, T, S, steps, extra=None, row_ids=None):
+    """Oracle draws of the selected rows at every decode step in `steps`
+    (offset = step for every row), one (step, row) pair per task so the workers
+    stay balanced. Returns (idx int64[len(steps), n], gap float64[len(steps), n])."""
+    B = logits.shape[0]
+    row_ids = np.arange(B) if row_ids is None else np.asarray(row_ids)
+    rows_c = {int(r): np.ascontiguousarray(logits[r]) for r in row_ids}
+    jobs = [(kind, rows_c[int(r)], dtype, float(T[r]), int(S[r]), int(r), int(s), extra or {})
+            for s in steps for r in row_ids]
+    res = list(pool().map(_row_job, jobs, chunksize=max(1, len(jobs) // 256)))
+    n = len(row_ids)
+    idx = np.array([r[0] for r in res], dtype=np.int64).reshape(len(steps), n)
+    gap = np.array([r[1] for r in res], dtype=np.float64).reshape(len(steps), n)
+    return idx, gap

@@ -9,7 +9,8 @@ import oracle
 import token_sampling_logits_gb300 as gs
 import workloads as W
 from tests import oracle_pool
-from tests.gpu_util import Tally, gpu_gumbel, gpu_hlg, rows_to_device, to_device
+from tests.gpu_util import (Tally, gpu_gumbel, gpu_gumbel_steps, register, rows_to_device,
+                            to_device)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -26,6 +27,8 @@ def _check_batch(batch, tally=None, rows=None, ctas=0, where="", cluster=0):
     ref, gap = _oracle_rows(batch, rows)
     t = tally or Tally()
     t.add(gpu[rows], ref, gap, greedy_mask=~(batch.temperature[rows] > 0), where=where)
+    if tally is None:
+        register("edge cases", t, assert_bound=False)
     return t
 
 
@@ -47,6 +50,7 @@ def test_small_shapes(dtype, B, V):
     t = Tally()
     for step in range(3):
         _check_batch(_small(B, V, dtype, seed=step), t, where="B=%d V=%d" % (B, V))
+    register("edge cases", t, assert_bound=False)
 
 
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
@@ -206,45 +210,55 @@ def test_workspace_left_clean_and_deterministic():
     assert not np.array_equal(a1, a3)
 
 
-@pytest.mark.parametrize("V", W.VOCAB_SWEEP)
-@pytest.mark.parametrize("B", W.BATCH_SWEEP)
-def test_sweep_workload(V, B):
-    base = W.sweep(V, B)
+def test_sweep_workload():
+    """The vocab x batch sweep at every one of its 1000 decode steps, every row:
+    39,000 rows against the oracle, under one near-tie bound for the config."""
+    steps = range(1000)
     t = Tally()
-    x = to_device(base.logits, base.dtype)
-    for step in (0, 1, 999):
-        b = base.at_step(step)
-        got = gpu_gumbel(b, logits_dev=x)
-        ref, gap = _oracle_rows(b)
-        t.add(got, ref, gap, where="sweep V=%d B=%d step %d" % (V, B, step))
+    for V in W.VOCAB_SWEEP:
+        for B in W.BATCH_SWEEP:
+            base = W.sweep(V, B)
+            got = gpu_gumbel_steps(base, steps)
+            ref, gap = oracle_pool.rows_at_steps("gumbel", base.logits, base.dtype,
+                                                 base.temperature, base.seed, steps)
+            t.add(got.ravel(), ref.ravel(), gap.ravel(), where="sweep V=%d B=%d" % (V, B))
+    register("2 sweep", t)
 
 
-@pytest.mark.parametrize("B", W.THROUGHPUT_B)
-def test_throughput_workload_sampled_rows(B):
-    """Full-size bf16 batches in the launch configuration the benchmark times;
-    the oracle scores a sample of rows one by one."""
-    base = W.throughput(B)
-    x = to_device(base.logits, base.dtype)
-    rows = np.unique(np.r_[0, B - 1, np.random.default_rng(B).choice(B, 14, replace=False)])
+def test_throughput_workload_all_rows():
+    """Full-size bf16 batches in the launch configuration the benchmark times:
+    every row of B = 64, 128 and 256 at 50 of the 100 decode steps (22,400 rows)."""
+    steps = list(range(0, 100, 2))
     t = Tally()
-    for step in (0, 57):
-        b = base.at_step(step)
-        got = gpu_gumbel(b, logits_dev=x)
-        ref, gap = _oracle_rows(b, rows)
-        t.add(got[rows], ref, gap, where="throughput B=%d step %d" % (B, step))
+    for B in W.THROUGHPUT_B:
+        base = W.throughput(B)
+        got = gpu_gumbel_steps(base, steps)
+        ref, gap = oracle_pool.rows_at_steps("gumbel", base.logits, base.dtype, base.temperature,
+                                             base.seed, steps)
+        t.add(got.ravel(), ref.ravel(), gap.ravel(), where="throughput B=%d" % B)
+    register("3 throughput", t)
 
 
 def test_mixed_greedy_workload():
+    """Every row of the mixed batch at 80 of its 100 steps: greedy rows byte-exact
+    (ties planted on rows 0, 2, 4, 6), sampled rows under the near-tie rule
+    (20,480 of them)."""
     base = W.mixed_greedy()
     x = to_device(base.logits, base.dtype)
     greedy = ~(base.temperature > 0)
-    for step in (0, 42):
-        b = base.at_step(step)
-        got = gpu_gumbel(b, logits_dev=x)
-        # every greedy row, byte-exact (ties planted on rows 0, 2, 4, 6)
-        gref, _ = oracle.argmax(b.logits, dtype=b.dtype)
-        assert np.array_equal(got[greedy], gref[greedy])
-        rows = np.r_[1, 3, 5, 7, np.random.default_rng(step).choice(np.arange(9, 512, 2), 12,
-                                                                     replace=False)]
-        ref, gap = _oracle_rows(b, rows)
-        Tally().add(got[rows], ref, gap, where="mixed step %d" % step)
+    steps = [s for s in range(100) if s % 5]
+    got = gpu_gumbel_steps(base, steps, logits_dev=x)
+    gref, _ = oracle.argmax(base.logits, dtype=base.dtype)
+    for k, s in enumerate(steps):
+        assert np.array_equal(got[k][greedy], gref[greedy]), "greedy rows differ at step %d" % s
+    sampled = np.flatnonzero(~greedy)
+    ref, gap = oracle_pool.rows_at_steps("gumbel", base.logits, base.dtype, base.temperature,
+                                         base.seed, steps, row_ids=sampled)
+    t = Tally()
+    t.add(got[:, sampled].ravel(), ref.ravel(), gap.ravel(), where="mixed")
+    register("5 mixed greedy (sampled rows)", t)
+    g = Tally()
+    g.add(got[:, greedy].ravel(), np.tile(gref[greedy], len(steps)),
+          np.zeros(greedy.sum() * len(steps)), greedy_mask=np.ones(greedy.sum() * len(steps), bool),
+          where="mixed greedy rows")
+    register("5 mixed greedy (greedy rows)", g, assert_bound=False)
