@@ -184,11 +184,15 @@ const char* gsample_status_string(gsample_status status);
  *   - The caller still passes the inputs and out_idx (same meaning as in
  *     gsample_gumbel_argmax); B > GSAMPLE_STATIC_WS_MAX_ROWS returns
  *     GSAMPLE_ERR_INVALID_ARG with nothing enqueued; B == 0 is a no-op.
+ *   - Every other argument is checked as gsample_gumbel_argmax checks it, and
+ *     a bad one returns that entry point's status with nothing enqueued.
  *   - The array is held by every GPU that loads the library until the process
- *     exits. The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) and zeroes it, synchronously; make that first call
- *     before any stream capture begins. A failed set-up returns
- *     GSAMPLE_ERR_CUDA.
+ *     exits, and is zero when the library's device code loads. The first call
+ *     on each device looks up its device address (cudaGetSymbolAddress) and
+ *     keeps it for the life of the process: do not call this entry point again
+ *     on a device after cudaDeviceReset. That first call must not be made while
+ *     `stream` is being captured: it returns GSAMPLE_ERR_UNSUPPORTED, with
+ *     nothing enqueued. A failed look-up returns GSAMPLE_ERR_CUDA.
  *   - Every call clears the rows it uses (an asynchronous memset on `stream`)
  *     before sampling, and calls no cudaMalloc, cudaFree or other allocating
  *     routine.

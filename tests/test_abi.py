@@ -180,3 +180,31 @@ def test_word_test_debug_entry_validation():
     assert call(T=float("nan")) == gs.ERR_INVALID_ARG
     assert call(x=None) == gs.ERR_INVALID_ARG
     assert call(flags=None) == gs.ERR_INVALID_ARG
+
+
+def test_static_workspace_entry_validation():
+    """gsample_gumbel_argmax_static checks every argument the regular entry point
+    checks before it sets anything up or enqueues anything (no device is touched
+    for a bad argument; on this CPU-only host a valid call fails at the device)."""
+    L = gs.lib()
+
+    def call(B=4, logits=FAKE, dtype=gs.F32, V=100, ld=100, T=FAKE, seed=FAKE, off=FAKE,
+             out=FAKE):
+        return L.gsample_gumbel_argmax_static(logits, dtype, B, V, ld, T, seed, off, out, None)
+
+    assert call(B=0) == gs.OK
+    assert call(B=-1) == gs.ERR_INVALID_ARG
+    assert call(B=4097) == gs.ERR_INVALID_ARG         # past the static array
+    assert call(logits=None) == gs.ERR_INVALID_ARG
+    assert call(out=None) == gs.ERR_INVALID_ARG
+    assert call(T=None) == gs.ERR_INVALID_ARG
+    assert call(seed=None) == gs.ERR_INVALID_ARG
+    assert call(off=None) == gs.ERR_INVALID_ARG
+    assert call(V=0) == gs.ERR_INVALID_ARG
+    assert call(ld=99) == gs.ERR_INVALID_ARG
+    assert call(dtype=7) == gs.ERR_INVALID_ARG
+    assert call(logits=FAKE + 2) == gs.ERR_INVALID_ARG  # f32 logits must be 4-byte aligned
+    assert call(out=FAKE + 4) == gs.ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call() == gs.ERR_CUDA

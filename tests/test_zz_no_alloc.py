@@ -27,7 +27,9 @@ def _call_static(x, T, S, O, out):
         torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("make", [lambda: W.mixed_greedy(B=96), lambda: W.sweep(65536, 8)])
+# Both batches take the flat split (more than 64 rows), whose merge state lives
+# in the shared array; smaller batches take a kernel that needs none.
+@pytest.mark.parametrize("make", [lambda: W.mixed_greedy(B=96), lambda: W.sweep(151936, 128)])
 def test_static_workspace_matches_caller_workspace(make):
     base = make()
     x = to_device(base.logits, base.dtype)
@@ -39,6 +41,25 @@ def test_static_workspace_matches_caller_workspace(make):
         ref = gs.gumbel_argmax(x, T, S, O)
         torch.cuda.synchronize()
         assert np.array_equal(out_static.cpu().numpy(), ref.cpu().numpy()), step
+
+
+def test_larger_batch_after_smaller_one():
+    """A call that uses more rows of the shared array than the call before it,
+    on the same stream: the rows the first call never touched must be cleared
+    like the others."""
+    small = W.throughput(80)
+    large = W.mixed_greedy(B=300)
+    xs = to_device(small.logits, small.dtype)
+    xl = to_device(large.logits, large.dtype)
+    for step in (3, 4):
+        for base, x in ((small, xs), (large, xl)):
+            b = base.at_step(step)
+            T, S, O = rows_to_device(b)
+            out_static = torch.full((b.B,), -7, dtype=torch.int64, device="cuda")
+            assert _call_static(x, T, S, O, out_static) == gs.OK
+            ref = gs.gumbel_argmax(x, T, S, O)
+            torch.cuda.synchronize()
+            assert np.array_equal(out_static.cpu().numpy(), ref.cpu().numpy()), (b.B, step)
 
 
 def test_static_workspace_size_limit():

@@ -415,6 +415,24 @@ gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64
 
 }  // namespace
 
+namespace gsample {
+
+// Every host-side check gsample_gumbel_argmax makes before it enqueues
+// anything, except the workspace's (the static-workspace entry point owns
+// its own): arguments, then the device.
+gsample_status validate_gumbel_args(const void* logits, gsample_dtype dtype, int64_t B,
+                                    int64_t V, int64_t ld, const float* temperature,
+                                    const uint64_t* seed, const uint64_t* offset,
+                                    const int64_t* out_idx) {
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, nullptr, false);
+  if (st != GSAMPLE_OK || B == 0) return st;
+  if (!temperature || !seed || !offset) return GSAMPLE_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  return device_info(&d);
+}
+
+}  // namespace gsample
+
 extern "C" {
 
 size_t gsample_workspace_bytes(int64_t B) {

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include "gsample.h"
 #include "gsample_device.cuh"
 
 namespace gsample {
@@ -112,6 +113,13 @@ cudaError_t launch_sample_cluster(const RowClusterParams& p, int dtype, bool vec
 int cat_max_cluster(int dtype, bool vec);
 size_t cat_smem_limit();
 cudaError_t launch_categorical(const RowClusterParams& p, int dtype, bool vec, cudaStream_t stream);
+
+// The host-side checks of gsample_gumbel_argmax other than the workspace's
+// (arguments, then the device), with nothing enqueued.
+gsample_status validate_gumbel_args(const void* logits, gsample_dtype dtype, int64_t B,
+                                    int64_t V, int64_t ld, const float* temperature,
+                                    const uint64_t* seed, const uint64_t* offset,
+                                    const int64_t* out_idx);
 
 cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, int64_t group0,
                                 int64_t n, uint32_t* out, cudaStream_t stream);
