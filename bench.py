@@ -58,6 +58,9 @@ def parse_args():
                     help="with --quick: time this workload instead of the headline (sweep takes "
                          "--batch and --vocab); prints a short line, for profiler runs")
     ap.add_argument("--vocab", type=int, default=151936, help="V of --workload sweep")
+    ap.add_argument("--count-blocks", action="store_true",
+                    help="build the block-counting variant of the library and print the Philox "
+                         "blocks the sampler computes per launch of the headline batch")
     ap.add_argument("--categorical", action="store_true",
                     help="with --workload: time the categorical (softmax + inverse-CDF) kernel")
     args = ap.parse_args()
@@ -121,29 +124,38 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# Integer-pipe roofline of Philox4x32-10. One block takes ten rounds of two
-# 32x32->64-bit products; the kernels fold the first two rounds' row-uniform
-# products into per-row constants, leaving 18 per block. A 64-bit product is
-# two 32-bit integer multiply-adds, and an SM retires 64 of those per clock
-# (the CUDA programming guide's throughput table for compute capability 9/10).
-PHILOX_PRODUCTS_PER_BLOCK = 18
-IMAD_PER_CLOCK_PER_SM = 64
+# Second roof of the sampler: the Philox4x32-10 blocks it computes, against the
+# measured rate of the library's own block code alone
+# (gsample_debug_philox_rate), at the best of a few occupancies.
+def philox_peak():
+    """Measured Philox blocks/s of the kernels' block code on this GPU."""
+    import torch
 
+    import token_sampling_logits_gb300 as gs
 
-def alu_peak(sms: int):
-    """Philox blocks per second that the integer multiply pipe allows at the
-    maximum SM clock (MEASURED_PEAKS.json's, else the part's 2070 MHz)."""
-    mhz = 2070.0
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            mhz = float(json.load(f).get("sm_max_mhz", mhz))
-    except Exception:
-        pass
-    per_sm_per_clock = IMAD_PER_CLOCK_PER_SM / 2.0 / PHILOX_PRODUCTS_PER_BLOCK
-    return sms * mhz * 1e6 * per_sm_per_clock, (
-        "derived: %d SMs x %.0f MHz x %d integer multiply-adds per clock per SM / 2 per "
-        "64-bit product / %d products per block" % (sms, mhz, IMAD_PER_CLOCK_PER_SM,
-                                                   PHILOX_PRODUCTS_PER_BLOCK))
+    L = gs.lib()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.empty(sms * 32 * 32, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    iters = 2000
+    best, best_w = 0.0, 0
+    for w in (8, 16, 24, 32):
+        times = []
+        for rep in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            rc = L.gsample_debug_philox_rate(w, iters, sink.data_ptr(), st)
+            e1.record()
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError("gsample_debug_philox_rate: " + gs.status_string(rc))
+            times.append(e0.elapsed_time(e1) * 1e-3)
+        rate = sms * w * 32 * iters * 4 / min(times)
+        if rate > best:
+            best, best_w = rate, w
+    return best, ("measured: gsample_debug_philox_rate (the kernels' four-way Philox block code "
+                  "alone), best of 8/16/24/32 warps per SM (%d), %d SMs" % (best_w, sms))
 
 
 class ClockSampler:
@@ -216,20 +228,26 @@ def kernel_source_hash(names=SAMPLE_KERNEL_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(profile_name: str, workload_rows: int):
-    """DRAM bytes per launch recorded by an ncu capture under profiles/, scaled
-    to the benchmark's batch; None when the kernel sources changed since."""
+def profile_figure(profile_name: str, key: str, workload_rows: int):
+    """A per-launch figure recorded under profiles/ (`key: value`, with the
+    kernel-source hash and the rows of the captured launch), scaled to the
+    benchmark's batch; None when the kernel sources changed since."""
     path = os.path.join(ROOT, "profiles", profile_name)
     try:
         text = open(path).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_val = re.search(r"%s:\s*([0-9.eE+]+)" % re.escape(key), text)
     m_rows = re.search(r"captured_rows:\s*(\d+)", text)
-    if not (m_hash and m_bytes and m_rows) or m_hash.group(1) != kernel_source_hash():
+    if not (m_hash and m_val and m_rows) or m_hash.group(1) != kernel_source_hash():
         return None
-    return float(m_bytes.group(1)) * workload_rows / int(m_rows.group(1))
+    return float(m_val.group(1)) * workload_rows / int(m_rows.group(1))
+
+
+def ncu_traffic(profile_name: str, workload_rows: int):
+    """DRAM bytes per launch of one ncu capture, scaled to the batch."""
+    return profile_figure(profile_name, "dram_bytes_per_launch", workload_rows)
 
 
 # ---------------------------------------------------------------------------
@@ -615,6 +633,13 @@ def run_case(args):
           flush=True)
 
 
+def headline_config(batch: W.Batch, world: int) -> dict:
+    """The workload both arms report (identical keys and values)."""
+    return {"workload": "throughput bf16 V=%d B=%d (N(0,4^2) + 32 Zipf(1.1) bumps of +6, "
+                        "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
+            "global_batch": batch.B * world, "vocab": batch.V}
+
+
 def run_ours(args, dist: Dist):
     import torch
 
@@ -652,18 +677,29 @@ def run_ours(args, dist: Dist):
     achieved = alg_bytes / (us_step * 1e-6) / 1e9
     peak, peak_kind = hbm_peak()
     # The method draws one Philox word per element: B * ceil(V / 4) blocks.
+    # The sampler computes fewer (exact pruning); a build of the library with
+    # -DGSAMPLE_COUNT_BLOCKS counts them (`bench.py --count-blocks`), and the
+    # count recorded under profiles/ is used while the kernel sources match.
     alg_blocks = batch.B * ((batch.V + 3) // 4)
-    blocks_per_s = alg_blocks / (us_step * 1e-6)
-    apeak, apeak_kind = alu_peak(props.multi_processor_count)
+    computed = profile_figure("sample_kernel_bf16_throughput.md", "philox_blocks_per_launch",
+                              batch.B)
+    ppeak, ppeak_kind = philox_peak() if not args.quick else (None, None)
     hbm_view = {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind + " (copy bandwidth)",
                 "floor_us": round(alg_bytes / (peak * 1e9) * 1e6, 2)}
-    alu_view = {"achieved": round(blocks_per_s, 1), "peak": round(apeak, 1),
-                "unit": "Philox4x32-10 blocks/s", "frac": round(blocks_per_s / apeak, 4),
-                "peak_kind": apeak_kind, "floor_us": round(alg_blocks / apeak * 1e6, 2)}
-    # The binding roof is the one with the longer floor time.
-    bound = "alu" if alu_view["floor_us"] > hbm_view["floor_us"] else "hbm"
-    main = alu_view if bound == "alu" else hbm_view
+    philox_view = None
+    if ppeak:
+        blocks = computed if computed is not None else float(alg_blocks)
+        philox_view = {
+            "achieved": round(blocks / (us_step * 1e-6), 1), "peak": round(ppeak, 1),
+            "unit": "Philox4x32-10 blocks/s", "frac": round(blocks / (us_step * 1e-6) / ppeak, 4),
+            "peak_kind": ppeak_kind,
+            "blocks_per_launch": round(blocks),
+            "blocks_kind": ("computed (device counter of a -DGSAMPLE_COUNT_BLOCKS build, "
+                            "recorded under profiles/)" if computed is not None else
+                            "algorithmic B * ceil(V/4) (no count recorded for these sources)"),
+            "algorithmic_blocks_per_launch": alg_blocks,
+            "floor_us": round(blocks / ppeak * 1e6, 2)}
 
     e2e = None
     if not args.quick:
@@ -693,23 +729,26 @@ def run_ours(args, dist: Dist):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "throughput bf16 V=%d B=%d (N(0,4^2) + 32 Zipf(1.1) bumps of +6, "
-                               "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
-                   "global_batch": batch.B * dist.world, "vocab": batch.V,
-                   "parallelism": "replicas x%d" % dist.world,
-                   "l2": "rotating pool of %d logits buffers (%.0f MB > 4 x L2 %.0f MB)" % (
-                       runner.P, runner.P * runner.bytes_per_step / 1e6, l2 / 1e6),
-                   "timing": "CUDA events around graph replays of %d launches" % runner.ring},
+        "config": headline_config(batch, dist.world),
+        "setup": {"parallelism": "replicas x%d" % dist.world,
+                  "l2": "rotating pool of %d logits buffers (%.0f MB > 4 x L2 %.0f MB): every "
+                        "step reads its input from DRAM" % (
+                            runner.P, runner.P * runner.bytes_per_step / 1e6, l2 / 1e6),
+                  "timing": "CUDA events around the %d timed launches, replayed from captured "
+                            "CUDA graphs of up to %d launches" % (args.steps, runner.ring)},
         "us_per_step": round(us_step, 3),
         "GBps": round(achieved, 1),
         "frac_of_8TBps": round(achieved / 8000.0, 4),
-        "roofline": {"bound": bound, "achieved": main["achieved"], "peak": main["peak"],
-                     "unit": main["unit"], "frac": main["frac"], "peak_kind": main["peak_kind"],
+        # The path streams each logit once: HBM bytes are the roof (the
+        # Philox view below explains the time the sampler spends above it).
+        "roofline": {"bound": "hbm", "achieved": hbm_view["achieved"], "peak": peak,
+                     "unit": "GB/s", "frac": hbm_view["frac"],
+                     "peak_kind": hbm_view["peak_kind"],
                      "traffic": ncu_traffic("sample_kernel_bf16_throughput.md", batch.B),
                      "kernel": "gsample::sample_kernel<bf16, 128-bit>",
                      "algorithmic_bytes_per_launch": alg_bytes,
-                     "algorithmic_blocks_per_launch": alg_blocks,
-                     "hbm": hbm_view, "alu": alu_view},
+                     "floor_us": hbm_view["floor_us"],
+                     "philox": philox_view},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
@@ -750,9 +789,8 @@ def run_reference(args, dist: Dist):
         "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(secs * 1000 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "throughput bf16 V=%d B=%d (N(0,4^2) + 32 Zipf(1.1) bumps of +6, "
-                               "T=1.0, splitmix64(7) seeds, offset=step)" % (batch.V, batch.B),
-                   "global_batch": batch.B, "vocab": batch.V, "parallelism": "host cores"},
+        "config": headline_config(batch, dist.world),
+        "setup": {"parallelism": "oracle on the host cores (rank 0)"},
         "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": cores,
                          "cpu": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
@@ -761,8 +799,52 @@ def run_reference(args, dist: Dist):
     print(json.dumps(line), flush=True)
 
 
+def run_count_blocks(args):
+    """Philox blocks the sampler computes per launch of the headline batch, from
+    a build of the library with a device counter (-DGSAMPLE_COUNT_BLOCKS, built
+    beside the regular one), at the headline temperature and two others."""
+    from token_sampling_logits_gb300 import build as gbuild
+
+    out_dir = os.path.join(ROOT, "token_sampling_logits_gb300", "_build", "count")
+    path = gbuild.build(extra_flags=["-DGSAMPLE_COUNT_BLOCKS"], out_dir=out_dir)
+    gbuild.LIB = path
+    gbuild.is_stale = lambda: False
+    import ctypes
+
+    import torch
+
+    import token_sampling_logits_gb300 as gs
+
+    L = gs.lib()
+    base = W.throughput(args.batch)
+    x = _to_device(base.logits, base.dtype)
+    S = gs.seeds_as_tensor(base.seed, "cuda")
+    cnt = ctypes.c_uint64(0)
+    res = {}
+    for T in (1.0, 0.3, 100.0):
+        Tt = torch.full((base.B,), T, dtype=torch.float32, device="cuda")
+        L.gsample_debug_blocks_computed(ctypes.byref(cnt), 1)
+        n = 20
+        for k in range(n):
+            gs.gumbel_argmax(x, Tt, S, torch.full((base.B,), k, dtype=torch.int64, device="cuda"))
+        torch.cuda.synchronize()
+        rc = L.gsample_debug_blocks_computed(ctypes.byref(cnt), 1)
+        if rc != 0:
+            raise RuntimeError("gsample_debug_blocks_computed: " + gs.status_string(rc))
+        res["T=%g" % T] = cnt.value / n
+    alg = base.B * ((base.V + 3) // 4)
+    print(json.dumps({"kernel_source_hash": kernel_source_hash(), "captured_rows": base.B,
+                      "algorithmic_blocks_per_launch": alg,
+                      "philox_blocks_per_launch": res,
+                      "share_of_algorithmic": {k: round(v / alg, 4) for k, v in res.items()}}),
+          flush=True)
+
+
 def main():
     args = parse_args()
+    if args.count_blocks:
+        run_count_blocks(args)
+        return
     dist = Dist(args.gpus)
     try:
         if args.impl == "reference":

@@ -70,6 +70,22 @@ gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dt
                                             int64_t* out_idx, int32_t cluster,
                                             gsample_stream_t stream);
 
+/* Philox4x32-10 throughput of the kernels' block code alone (Salmon et al.,
+ * SC'11; the row-folded first two rounds and four blocks per thread side by
+ * side, as in the sampler). One CTA per SM of warps_per_sm warps (1..32); each
+ * thread computes 4 * iters blocks and folds their words into sink[thread].
+ * sink: device uint32[SMs * warps_per_sm * 32]. Time it on `stream` to get the
+ * measured Philox rate the sampler's second roofline is reported against. */
+gsample_status gsample_debug_philox_rate(int32_t warps_per_sm, uint32_t iters, uint32_t* sink,
+                                         gsample_stream_t stream);
+
+/* Philox blocks the row sampler computed since the last reset (dense tiles,
+ * compacted batches, first candidates and exact passes, summed over
+ * launches), in a library built with -DGSAMPLE_COUNT_BLOCKS; reset != 0 sets
+ * the count back to zero after reading it. The regular build returns
+ * GSAMPLE_ERR_UNSUPPORTED. Synchronous (reads a device counter). */
+gsample_status gsample_debug_blocks_computed(uint64_t* count, int32_t reset);
+
 /* Number of CTAs the library would launch for this problem (0 on bad args). */
 int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
                                    const void* logits, int32_t hlg);

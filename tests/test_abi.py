@@ -208,3 +208,18 @@ def test_static_workspace_entry_validation():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         assert call() == gs.ERR_CUDA
+
+
+def test_philox_rate_and_block_counter_validation():
+    L = gs.lib()
+    assert L.gsample_debug_philox_rate(0, 10, FAKE, None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_philox_rate(33, 10, FAKE, None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_philox_rate(8, 0, FAKE, None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_philox_rate(8, 10, None, None) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_blocks_computed(None, 0) == gs.ERR_INVALID_ARG
+    # the regular build has no counter
+    c = ctypes.c_uint64(7)
+    assert L.gsample_debug_blocks_computed(ctypes.byref(c), 0) == gs.ERR_UNSUPPORTED
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert L.gsample_debug_philox_rate(8, 10, FAKE, None) == gs.ERR_CUDA

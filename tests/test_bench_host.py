@@ -5,6 +5,7 @@ import importlib.util
 import os
 import socket
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -84,18 +85,30 @@ def test_stored_traffic_is_scaled_and_nulled_on_source_change(tmp_path, monkeypa
     assert b.ncu_traffic("missing.md", 30) is None
 
 
-def test_integer_pipe_peak_from_unit_counts():
+def test_recorded_block_count_is_scaled_and_nulled_on_source_change(tmp_path, monkeypatch):
     b = _bench()
-    peak, kind = b.alu_peak(152)
-    # 152 SMs x 2070 MHz x 64 / 2 / 18
-    import json
+    h = b.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1000\n"
+                               "philox_blocks_per_launch: 640\ncaptured_rows: 10\n" % h)
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: h)
+    assert b.profile_figure("p.md", "philox_blocks_per_launch", 20) == pytest.approx(1280.0)
+    assert b.profile_figure("p.md", "not_recorded", 20) is None
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: "0" * 16)
+    assert b.profile_figure("p.md", "philox_blocks_per_launch", 20) is None
 
-    try:
-        mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
-    except (OSError, KeyError, ValueError):
-        mhz = 2070.0
-    assert peak == pytest.approx(152 * mhz * 1e6 * 64 / 2 / 18, rel=1e-9)
-    assert kind.startswith("derived")
+
+def test_headline_config_is_shared_by_both_arms():
+    b = _bench()
+    import workloads as W
+
+    batch = W.Batch("t", np.zeros((4, 8), np.uint16), W.BF16, np.ones(4, np.float32),
+                    np.zeros(4, np.uint64), np.zeros(4, np.uint64))
+    c = b.headline_config(batch, 2)
+    assert set(c) == {"workload", "global_batch", "vocab"}
+    assert c["global_batch"] == 8 and c["vocab"] == 8
 
 
 def test_side_workload_needs_quick(monkeypatch):

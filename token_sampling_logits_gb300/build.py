@@ -46,15 +46,21 @@ def is_stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile the library (if stale, or forced). With out_dir, a variant with
+    extra_flags (e.g. -DGSAMPLE_COUNT_BLOCKS) is built there instead, always,
+    leaving the regular library alone; returns the path of the built .so."""
+    lib_path = LIB if out_dir is None else os.path.join(out_dir, "libgsample.so")
+    obj_dir = OBJ_DIR if out_dir is None else out_dir
+    if out_dir is None and not force and not is_stale():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -67,13 +73,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=max(1, len(sources()))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib_path + ".tmp.%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

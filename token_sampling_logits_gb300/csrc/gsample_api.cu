@@ -548,6 +548,34 @@ gsample_status gsample_debug_philox(uint64_t seed, uint32_t row, uint64_t offset
   return GSAMPLE_OK;
 }
 
+gsample_status gsample_debug_philox_rate(int32_t warps_per_sm, uint32_t iters, uint32_t* sink,
+                                         gsample_stream_t stream) {
+  if (warps_per_sm < 1 || warps_per_sm > 32 || iters < 1 || !sink || (uintptr_t)sink % 4)
+    return GSAMPLE_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  const gsample_status st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  if (gsample::launch_debug_philox_rate(d->sms, warps_per_sm * 32, iters, sink,
+                                        (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
+gsample_status gsample_debug_blocks_computed(uint64_t* count, int32_t reset) {
+  if (!count) return GSAMPLE_ERR_INVALID_ARG;
+  unsigned long long v = 0;
+  const cudaError_t e = gsample::read_blocks_computed(&v, reset != 0);
+  if (e == cudaErrorNotSupported) return GSAMPLE_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  *count = v;
+  return GSAMPLE_OK;
+}
+
 gsample_status gsample_debug_gumbel(const uint32_t* words, int64_t n, float* gumbel, float* bound,
                                     gsample_stream_t stream) {
   if (n < 0 || !words || !gumbel) return GSAMPLE_ERR_INVALID_ARG;

@@ -125,6 +125,10 @@ cudaError_t launch_debug_philox(uint64_t seed, uint32_t row, uint64_t offset, in
                                 int64_t n, uint32_t* out, cudaStream_t stream);
 cudaError_t launch_debug_word_test(const float* x, const uint32_t* w, int64_t n, float L, float T,
                                    uint32_t* threshold, uint8_t* flags, cudaStream_t stream);
+cudaError_t launch_debug_philox_rate(int ctas, int threads, uint32_t iters, uint32_t* sink,
+                                     cudaStream_t stream);
+// Blocks counted by a GSAMPLE_COUNT_BLOCKS build; cudaErrorNotSupported otherwise.
+cudaError_t read_blocks_computed(unsigned long long* out, bool reset);
 cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, float* bound,
                                 cudaStream_t stream);
 

@@ -40,6 +40,23 @@
 #include "gsample_internal.h"
 
 namespace gsample {
+
+#ifdef GSAMPLE_COUNT_BLOCKS
+// Diagnostic builds only: Philox blocks the sampler computed, summed over
+// launches (dense tiles, compacted batches, first candidates, exact passes).
+__device__ unsigned long long g_blocks_computed;
+#define GSAMPLE_COUNT(n)                                                          \
+  do {                                                                            \
+    const unsigned long long c_ = (unsigned long long)__reduce_add_sync(          \
+        0xFFFFFFFFu, (unsigned)(n));                                              \
+    if ((threadIdx.x & 31) == 0) atomicAdd(&g_blocks_computed, c_);               \
+  } while (0)
+#else
+#define GSAMPLE_COUNT(n) \
+  do {                   \
+  } while (0)
+#endif
+
 namespace {
 
 #ifndef GSAMPLE_VPT
@@ -347,6 +364,7 @@ __device__ __noinline__ Best flush_rare_cold(const unsigned char* rbase, int rcn
                                              PhiloxRow ph, Prune pr, float bs, int32_t bi) {
   const int lane = threadIdx.x & 31;
   __syncwarp();  // the entries of every lane are visible
+  GSAMPLE_COUNT(lane < rcnt ? 1 : 0);
   if (lane < rcnt) {
     const uint32_t g = reinterpret_cast<const uint32_t*>(rbase)[lane];
     float x[4];
@@ -452,6 +470,14 @@ __device__ __forceinline__ void compact_batch(uint32_t stage, const unsigned sho
   }
   uint4 w[N];
   philox_row_xn<N>(g, rc.ph, w);
+#ifdef GSAMPLE_COUNT_BLOCKS
+  {
+    int nv = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) nv += valid[j] ? 1 : 0;
+    GSAMPLE_COUNT(nv);
+  }
+#endif
   uint32_t need = 0;
 #pragma unroll
   for (int j = 0; j < N; ++j) need |= (valid[j] && max_word(w[j]) >= wt[j]) ? (1u << j) : 0u;
@@ -514,6 +540,7 @@ __device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const 
 #pragma unroll
     for (int i = 0; i < NG; ++i) wt[i] = word_threshold(xm[i], pr, rt);
     uint32_t need = 0;
+    GSAMPLE_COUNT(NG);
     const uint32_t gl = g0 + lane_group<DT, VEC>(0, lane);
 #pragma unroll
     for (int b = 0; b < NG; b += 4) {
@@ -580,6 +607,7 @@ __device__ __forceinline__ void lane_candidate(uint32_t stage, int32_t t0, int32
       ck = k;
     }
   }
+  GSAMPLE_COUNT(ck < 0 ? 0 : 1);
   if (ck < 0) return;
   const uint4 ru = lds128(stage + (uint32_t)(ck * 32 + lane) * 16u);
   int ce = C::kEPU - 1;
@@ -915,6 +943,25 @@ __global__ void debug_word_test_kernel(const float* x, const uint32_t* w, int64_
   }
 }
 
+// Philox throughput alone: each thread runs `iters` batches of four blocks of
+// the kernels' row-folded block code (philox_row_x4) and folds the words into
+// sink[thread], so nothing but the blocks is measured.
+__global__ void __launch_bounds__(1024, 1) debug_philox_rate_kernel(uint32_t iters, uint32_t* sink) {
+  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  const PhiloxRow pr = philox_row(blockIdx.x, 7u, 0u, 0x12345u + t / 1024u, 0x6789Au);
+  uint32_t acc = 0;
+  for (uint32_t it = 0; it < iters; ++it) {
+    uint32_t g[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g[j] = t * 4096u + it * 4u + (uint32_t)j;
+    uint4 w[4];
+    philox_row_x4(g, pr, w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc ^= w[j].x ^ w[j].y ^ w[j].z ^ w[j].w;
+  }
+  sink[t] = acc;
+}
+
 unsigned grid_for(int64_t n) {
   const int64_t blocks = (n + 255) / 256;
   return (unsigned)(blocks < 4096 ? (blocks < 1 ? 1 : blocks) : 4096);
@@ -932,6 +979,27 @@ cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, floa
                                 cudaStream_t stream) {
   debug_gumbel_kernel<<<grid_for(n), 256, 0, stream>>>(words, n, g, bound);
   return cudaGetLastError();
+}
+
+cudaError_t launch_debug_philox_rate(int ctas, int threads, uint32_t iters, uint32_t* sink,
+                                     cudaStream_t stream) {
+  debug_philox_rate_kernel<<<ctas, threads, 0, stream>>>(iters, sink);
+  return cudaGetLastError();
+}
+
+cudaError_t read_blocks_computed(unsigned long long* out, bool reset) {
+#ifdef GSAMPLE_COUNT_BLOCKS
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_blocks_computed, sizeof *out);
+  if (e == cudaSuccess && reset) {
+    const unsigned long long z = 0;
+    e = cudaMemcpyToSymbol(g_blocks_computed, &z, sizeof z);
+  }
+  return e;
+#else
+  (void)out;
+  (void)reset;
+  return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t launch_debug_word_test(const float* x, const uint32_t* w, int64_t n, float L, float T,
