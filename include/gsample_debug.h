@@ -86,6 +86,15 @@ gsample_status gsample_debug_philox_rate(int32_t warps_per_sm, uint32_t iters, u
  * GSAMPLE_ERR_UNSUPPORTED. Synchronous (reads a device counter). */
 gsample_status gsample_debug_blocks_computed(uint64_t* count, int32_t reset);
 
+/* The HLG kernel's exact candidate score ("HLG sampling", "The transfer
+ * function"): out[j] = tone(x[j] + shift) / T + g(words[j]) in binary32, the
+ * tone curve of `hlg` (pivot fields unused), the shift standing for the row's
+ * pivot (z = x + shift). x, words, out: device arrays of n entries; T > 0 and
+ * shift finite, else GSAMPLE_ERR_INVALID_ARG. */
+gsample_status gsample_debug_hlg_score(const float* x, const uint32_t* words, int64_t n,
+                                       const gsample_hlg_params* hlg, float T, float shift,
+                                       float* out, gsample_stream_t stream);
+
 /* Number of CTAs the library would launch for this problem (0 on bad args). */
 int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,
                                    const void* logits, int32_t hlg);

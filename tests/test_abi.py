@@ -223,3 +223,20 @@ def test_philox_rate_and_block_counter_validation():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         assert L.gsample_debug_philox_rate(8, 10, FAKE, None) == gs.ERR_CUDA
+
+
+def test_hlg_score_debug_validation():
+    L = gs.lib()
+    hp = gs.HlgParams().to_c()
+    bad = gs.HlgParams(m=-1.0).to_c()
+    st = None
+    assert L.gsample_debug_hlg_score(FAKE, FAKE, 4, ctypes.byref(hp), 0.0, 1.0, FAKE, st) == \
+        gs.ERR_INVALID_ARG                                             # T must be > 0
+    assert L.gsample_debug_hlg_score(FAKE, FAKE, 4, ctypes.byref(hp), 1.0, float("inf"), FAKE,
+                                     st) == gs.ERR_INVALID_ARG         # shift must be finite
+    assert L.gsample_debug_hlg_score(FAKE, FAKE, 4, ctypes.byref(bad), 1.0, 1.0, FAKE, st) == \
+        gs.ERR_INVALID_ARG
+    assert L.gsample_debug_hlg_score(FAKE, FAKE, 4, None, 1.0, 1.0, FAKE, st) == gs.ERR_INVALID_ARG
+    assert L.gsample_debug_hlg_score(None, FAKE, 4, ctypes.byref(hp), 1.0, 1.0, FAKE, st) == \
+        gs.ERR_INVALID_ARG
+    assert L.gsample_debug_hlg_score(FAKE, FAKE, 0, ctypes.byref(hp), 1.0, 1.0, FAKE, st) == gs.OK

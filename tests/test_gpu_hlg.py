@@ -1,6 +1,8 @@
 """HLG kernel vs the CPU oracle on the hlg workload recipe and edge cases,
 plus the pages' neutrality gate on the GPU ("HLG sampling", "The degeneracies
 are the safety anchors", "Correctness & evaluation" 1)."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -176,3 +178,44 @@ def test_hlg_per_row_invalid_curve_gives_minus_one():
     assert got[2] == int(np.argmax(x[2]))         # a greedy row ignores its curve
     ref, gap = _rows_oracle(b, [curves[0]] * B)
     Tally().add(got[:1], ref[:1], gap[:1], where="valid row beside invalid ones")
+
+
+def test_hlg_score_error_budget():
+    """The kernel's exact HLG score tone(x + shift)/T + g against the oracle's
+    double-precision curve and Gumbel transform, over all three branches of the
+    curve ("HLG sampling", "The transfer function"), within the binary32 budget
+    of every step: the rounded z (at most half an ulp of z, times the slope m),
+    the curve's own arithmetic (at most 4 ulps of the curve value), the IEEE
+    division by T (half an ulp), the Gumbel transform (2e-6, its pinned bound
+    over all 2^23 cells) and the final sum (half an ulp of the score)."""
+    rng = np.random.default_rng(77)
+    n = 1_000_000
+    f32 = np.float32
+    for T in (1.0, 0.7, 1.6):
+        m, w, bt, bh = 1.3, 2.0, 1.0, 1.5
+        shift = f32(6.0 - rng.uniform(5, 25))           # c - M for a range of row maxima
+        z = np.concatenate([rng.uniform(-60, 12, n // 2), rng.uniform(-w - 1, w + 1, n // 2)])
+        x = (z - np.float64(shift)).astype(f32)
+        words = rng.integers(0, 2**32, n, dtype=np.uint64).astype(np.uint32)
+        words[:64] = np.arange(64, dtype=np.uint32) | np.uint32(0xFFFFFF00)  # largest g
+        xd = torch.from_numpy(x).cuda()
+        wd = torch.from_numpy(words.view(np.int32)).cuda()
+        out = torch.empty(n, dtype=torch.float32, device="cuda")
+        hp = gs.HlgParams(m=m, w=w, beta_t=bt, beta_h=bh).to_c()
+        rc = gs.lib().gsample_debug_hlg_score(xd.data_ptr(), wd.data_ptr(), n,
+                                              ctypes.byref(hp), T, float(shift), out.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+        assert rc == gs.OK
+        got = out.cpu().numpy().astype(np.float64)
+        zd = x.astype(np.float64) + np.float64(shift)
+        y = oracle.hlg_curve(zd, m, w, bt, bh)
+        Tq = np.float64(f32(T))
+        ref = y / Tq + oracle.gumbel_of_words(words)
+        ulp = lambda v: np.spacing(np.abs(v).astype(f32)).astype(np.float64)  # noqa: E731
+        zf = x.astype(f32) + f32(shift)                   # the kernel's rounded z
+        bound = (m * 0.5 * ulp(zf) + 4 * ulp(y)) / Tq + 0.5 * ulp(y / Tq) + 2e-6 + 0.5 * ulp(ref)
+        err = np.abs(got - ref)
+        worst = int(np.argmax(err / bound))
+        print("T=%g: max |score error| %.2e, largest share of the budget %.2f" %
+              (T, err.max(), (err / bound).max()))
+        assert (err <= bound).all(), (T, float(z[worst]), float(err[worst]), float(bound[worst]))

@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
             "gsample_debug_planned_ctas": (_i32, [_int, _i64, _i64, _i64, _vp, _i32]),
             "gsample_debug_philox_rate": (_int, [_i32, _u32, _vp, _vp]),
             "gsample_debug_blocks_computed": (_int, [_vp, _i32]),
+            "gsample_debug_hlg_score": (_int, [_vp, _vp, _i64, _vp, ctypes.c_float, ctypes.c_float,
+                                               _vp, _vp]),
             "gsample_gumbel_argmax_static": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                     _vp, _vp]),
             "gsample_gumbel_argmax_host": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,

@@ -563,6 +563,24 @@ gsample_status gsample_debug_philox_rate(int32_t warps_per_sm, uint32_t iters, u
   return GSAMPLE_OK;
 }
 
+gsample_status gsample_debug_hlg_score(const float* x, const uint32_t* words, int64_t n,
+                                       const gsample_hlg_params* hlg, float T, float shift,
+                                       float* out, gsample_stream_t stream) {
+  if (n < 0 || !(T > 0.0f) || !isfinite(shift)) return GSAMPLE_ERR_INVALID_ARG;
+  if (check_hlg(hlg) != GSAMPLE_OK) return GSAMPLE_ERR_INVALID_ARG;
+  if (n == 0) return GSAMPLE_OK;
+  if (!x || !words || !out) return GSAMPLE_ERR_INVALID_ARG;
+  const DeviceInfo* d = nullptr;
+  const gsample_status st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  if (gsample::launch_debug_hlg_score(x, words, n, hlg->m, hlg->w, hlg->beta_t, hlg->beta_h, T,
+                                      shift, out, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
 gsample_status gsample_debug_blocks_computed(uint64_t* count, int32_t reset) {
   if (!count) return GSAMPLE_ERR_INVALID_ARG;
   unsigned long long v = 0;

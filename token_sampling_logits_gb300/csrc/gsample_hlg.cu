@@ -115,11 +115,14 @@ struct RowState {
   bool pinf;     // the row holds a +inf logit: only +inf entries can win
 };
 
+// The exact score tone(z)/T + g, with an IEEE division as the oracle reads
+// "tone(z) / T" (only scored candidates pay for it; pruning multiplies by 1/T
+// inside its slack).
 __device__ __forceinline__ float hlg_score(const Curve& c, const RowState& rs, float x,
-                                           uint32_t word, float rT) {
+                                           uint32_t word, float T) {
   if (x == INFINITY) return INFINITY;
   const float y = tone(c, x + rs.shift);
-  return y * rT + gumbel_of_word(word);
+  return __fdiv_rn(y, T) + gumbel_of_word(word);
 }
 
 // Block-wide (score, index) argmax; every thread gets the result. `red` holds
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
     // best of them is the bound L that sweep 2 prunes against.
     if (cand_i != INT32_MAX && cand_x > -INFINITY && (!rs.pinf || cand_x == INFINITY)) {
       const uint4 blk = philox_row_1((uint32_t)cand_i >> 2, ph);
-      take_better(hlg_score(cv, rs, cand_x, word_of(blk, cand_i & 3), rT), cand_i, bs, bi);
+      take_better(hlg_score(cv, rs, cand_x, word_of(blk, cand_i & 3), T), cand_i, bs, bi);
     }
     // The bound: the best first candidate of the whole row, over the cluster.
     {
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
           if (word_test &&
               !may_reach(tone_upper(cv, x + rs.shift), word_of(ww, t), ReachTest{wa, wc}))
             continue;
-          take_better(hlg_score(cv, rs, x, word_of(ww, t), rT), (int32_t)(4 * gg + t), bs, bi);
+          take_better(hlg_score(cv, rs, x, word_of(ww, t), T), (int32_t)(4 * gg + t), bs, bi);
         }
       }
       __syncwarp();
@@ -464,7 +467,27 @@ void* select_hlg(int dtype, bool vec, bool resident) {
 
 constexpr size_t kSmemLimit = 204 * 1024;  // leaves room for the static shared variables
 
+// Diagnostics: the exact HLG score of given logits and words with a given
+// shift (z = x + shift), as the kernel scores its candidates.
+__global__ void debug_hlg_score_kernel(const float* x, const uint32_t* words, int64_t n, Curve c,
+                                       float T, float shift, float* out) {
+  const RowState rs{shift, false};
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+       j += (int64_t)gridDim.x * blockDim.x)
+    out[j] = hlg_score(c, rs, x[j], words[j], T);
+}
+
 }  // namespace
+
+cudaError_t launch_debug_hlg_score(const float* x, const uint32_t* words, int64_t n, float m,
+                                   float w, float beta_t, float beta_h, float T, float shift,
+                                   float* out, cudaStream_t stream) {
+  const Curve c{m, w, beta_t, beta_h, 1.0f / beta_t, 1.0f / beta_h};
+  const int64_t blocks = (n + 255) / 256;
+  debug_hlg_score_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+      x, words, n, c, T, shift, out);
+  return cudaGetLastError();
+}
 
 size_t hlg_smem_limit() { return kSmemLimit; }
 

@@ -129,6 +129,9 @@ cudaError_t launch_debug_philox_rate(int ctas, int threads, uint32_t iters, uint
                                      cudaStream_t stream);
 // Blocks counted by a GSAMPLE_COUNT_BLOCKS build; cudaErrorNotSupported otherwise.
 cudaError_t read_blocks_computed(unsigned long long* out, bool reset);
+cudaError_t launch_debug_hlg_score(const float* x, const uint32_t* words, int64_t n, float m,
+                                   float w, float beta_t, float beta_h, float T, float shift,
+                                   float* out, cudaStream_t stream);
 cudaError_t launch_debug_gumbel(const uint32_t* words, int64_t n, float* g, float* bound,
                                 cudaStream_t stream);
 
