@@ -85,6 +85,12 @@ def _load():
                                               _vp, _vp]),
             "oracle_categorical": (None, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
                                           _vp, _vp]),
+            "oracle_filtered_sample_row": (_i64, [_vp, _int, _i64, _flt, _u64, _u32, _u64,
+                                                  ctypes.c_int32, _flt, _vp, _vp]),
+            "oracle_filtered_gumbel_argmax": (None, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                     _vp, _vp, _vp, _vp, _vp]),
+            "oracle_filtered_steps": (None, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _u64, _i64,
+                                             _vp, _vp, _vp]),
             "oracle_philox_blocks": (None, [_u32, _u32, _vp, _i64, _vp]),
             "oracle_stream_words": (None, [_u64, _u32, _u64, _i64, _i64, _vp]),
             "oracle_gumbel_of_words": (None, [_vp, _i64, _vp]),
@@ -337,3 +343,52 @@ def hlg_gumbel_argmax(logits: np.ndarray, temperature, seed, offset, m, w, beta_
                                  _ptr(pw), _ptr(pbt), _ptr(pbh), _ptr(pc), _ptr(pmode), _ptr(idx),
                                  _ptr(gap))
     return idx, gap
+
+
+def filtered_sample_row(row: np.ndarray, temperature: float, seed: int, row_id: int,
+                        offset: int, top_k: int = 0, top_p: float = 1.0,
+                        dtype: int | None = None):
+    """Top-k / top-p Gumbel-max sample of one row (see oracle.c, [FILTER]).
+    -> (idx, gap within the filter set, nucleus edge margin)."""
+    lib = _load()
+    row = np.ascontiguousarray(row)
+    dt = _dtype_code(row, dtype)
+    gap = ctypes.c_double()
+    edge = ctypes.c_double()
+    idx = lib.oracle_filtered_sample_row(_ptr(row), dt, row.size, temperature, seed, row_id,
+                                         offset, int(top_k), float(top_p), ctypes.byref(gap),
+                                         ctypes.byref(edge))
+    return int(idx), gap.value, edge.value
+
+
+def filtered_gumbel_argmax(logits: np.ndarray, temperature, seed, offset, top_k=0, top_p=1.0,
+                           dtype: int | None = None):
+    """Per-row top-k / top-p Gumbel-max. -> (idx int64[B], gap float64[B], edge float64[B])."""
+    lib = _load()
+    x, B, V, ld = _logits_2d(logits)
+    dt = _dtype_code(x, dtype)
+    T, S, O = _row_arrays(B, temperature, seed, offset)
+    K = np.ascontiguousarray(np.broadcast_to(np.asarray(top_k, dtype=np.int32), (B,)))
+    P = np.ascontiguousarray(np.broadcast_to(np.asarray(top_p, dtype=np.float32), (B,)))
+    idx = np.zeros(B, dtype=np.int64)
+    gap = np.zeros(B, dtype=np.float64)
+    edge = np.zeros(B, dtype=np.float64)
+    lib.oracle_filtered_gumbel_argmax(_ptr(x), dt, B, V, ld, _ptr(T), _ptr(S), _ptr(O), _ptr(K),
+                                      _ptr(P), _ptr(idx), _ptr(gap), _ptr(edge))
+    return idx, gap, edge
+
+
+def filtered_steps(logits: np.ndarray, temperature, seed, base_offset: int, steps: int,
+                   top_k=0, top_p=1.0, dtype: int | None = None):
+    """steps decode steps of a filtered batch -> idx int64[steps, B]."""
+    lib = _load()
+    x, B, V, ld = _logits_2d(logits)
+    dt = _dtype_code(x, dtype)
+    T = np.ascontiguousarray(np.broadcast_to(np.asarray(temperature, dtype=np.float32), (B,)))
+    S = np.ascontiguousarray(np.broadcast_to(np.asarray(seed, dtype=np.uint64), (B,)))
+    K = np.ascontiguousarray(np.broadcast_to(np.asarray(top_k, dtype=np.int32), (B,)))
+    P = np.ascontiguousarray(np.broadcast_to(np.asarray(top_p, dtype=np.float32), (B,)))
+    idx = np.zeros((steps, B), dtype=np.int64)
+    lib.oracle_filtered_steps(_ptr(x), dt, B, V, ld, _ptr(T), _ptr(S), base_offset, steps,
+                              _ptr(K), _ptr(P), _ptr(idx))
+    return idx

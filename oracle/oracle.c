@@ -19,6 +19,9 @@
  *   [PHILOX]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *             1, 2, 3", SC'11, section 3 (the Philox round function and the
  *             Weyl key schedule) -- the published definition of Philox4x32-10.
+ *   [FILTER]  The same issue, Background: rejection-based top-k / top-p on the
+ *             Gumbel path is named as the follow-up work; see the reading in
+ *             the section of that name below.
  *   [HLG]     "HLG sampling -- a piecewise tone curve on the logits" (mlx-bun
  *             docs/design/hlg-sampling.md), sections "The transfer function",
  *             "The pivot", "Greedy is untouched", "Temperature semantics".
@@ -43,6 +46,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_F32 0
@@ -484,6 +488,149 @@ void oracle_categorical(const void* logits, int dtype, int64_t B, int64_t V, int
                                         out_probe_dist ? &out_probe_dist[b] : NULL,
                                         out_margin ? &out_margin[b] : NULL);
   }
+}
+
+/* ----------------------------------------------------------------------------
+ * [FILTER] Top-k / top-p (nucleus) sampling on the Gumbel path. The issue
+ * names "rejection-based top-k/top-p" on Gumbel-max as its follow-up without
+ * specifying it. Reading:
+ *   - the candidates (logits that are neither NaN nor -inf) are ordered by
+ *     logit, larger first, equal logits by lower index;
+ *   - the filter set K is the first r of that order, r = min(r_k, r_p):
+ *       r_k = top_k when top_k >= 1 (at most the number of candidates), else
+ *             every candidate;
+ *       r_p = the smallest r whose softmax(x / T) mass reaches top_p * S
+ *             (S = the total mass) when top_p < 1; r_p = 1 when top_p <= 0;
+ *             every candidate when top_p >= 1 or NaN. A row with +inf logits
+ *             gives each +inf entry mass 1 and every other entry 0;
+ *   - the sample is the Gumbel-max over K alone, with the same per-element
+ *     noise: argmax over i in K of x_i / T + g_i, lowest index on ties. The
+ *     Gumbel-max property holds on any subset, so this is an exact draw of
+ *     softmax(x / T) restricted to K.
+ * "Rejection": the unrestricted Gumbel-max draw is a proposal; when it lies
+ * in K it is also the argmax over K (the maximum over a superset that falls in
+ * the subset), so it is kept, and only otherwise is K needed. Both give the
+ * index defined above, which is what this function computes directly: a
+ * library sort of the candidates, the prefix, then the restricted argmax.
+ * Temperature <= 0 or NaN: greedy argmax (the filters keep the top element).
+ * Outputs: gap = the top-two score gap within K (as oracle_sample_row);
+ * edge = how far the nucleus boundary is from moving by one element, relative
+ * to S: min((cum_r - p S) / S, (p S - cum_{r-1}) / S) at r = r_p, or +inf when
+ * the nucleus does not decide K (top_p inactive, or r_k < r_p).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int64_t idx;
+  double x;
+} filt_cand_t;
+
+static int filt_order(const void* a, const void* b) {
+  const filt_cand_t* p = (const filt_cand_t*)a;
+  const filt_cand_t* q = (const filt_cand_t*)b;
+  if (p->x > q->x) return -1;
+  if (p->x < q->x) return 1;
+  return p->idx < q->idx ? -1 : (p->idx > q->idx ? 1 : 0);
+}
+
+int64_t oracle_filtered_sample_row(const void* row, int dtype, int64_t V, float temperature,
+                                   uint64_t seed, uint32_t row_id, uint64_t offset,
+                                   int32_t top_k, float top_p, double* gap, double* edge) {
+  double T = (double)temperature;
+  if (edge) *edge = INFINITY;
+  if (!(T > 0.0)) return greedy_row(row, dtype, V, gap);
+  filt_cand_t* c = (filt_cand_t*)malloc((size_t)(V > 0 ? V : 1) * sizeof(filt_cand_t));
+  int64_t n = 0, n_inf = 0;
+  double M = -INFINITY;
+  for (int64_t i = 0; i < V; ++i) {
+    double x = oracle_load(row, dtype, i);
+    if (isnan(x) || x == -INFINITY) continue;
+    c[n].idx = i;
+    c[n].x = x;
+    ++n;
+    if (x == INFINITY) ++n_inf;
+    if (x > M) M = x;
+  }
+  if (n == 0) {
+    free(c);
+    if (gap) *gap = INFINITY;
+    return -1;
+  }
+  qsort(c, (size_t)n, sizeof(filt_cand_t), filt_order);
+  int64_t r_k = (top_k >= 1 && (int64_t)top_k < n) ? (int64_t)top_k : n;
+  int64_t r_p = n;
+  double p = (double)top_p;
+  if (p <= 0.0) {
+    r_p = 1;
+  } else if (p < 1.0) {
+    double S = 0.0;
+    for (int64_t j = 0; j < n; ++j)
+      S += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
+    double cum = 0.0, before = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      before = cum;
+      cum += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
+      if (cum >= p * S) {
+        r_p = j + 1;
+        break;
+      }
+    }
+    if (edge && r_p <= r_k) *edge = fmin((cum - p * S) / S, (p * S - before) / S);
+  }
+  int64_t r = r_k < r_p ? r_k : r_p;
+  /* The restricted argmax, visiting K in index order so that only a strictly
+   * larger score replaces the best (lowest index on ties). */
+  int64_t* in_k = (int64_t*)malloc((size_t)r * sizeof(int64_t));
+  for (int64_t j = 0; j < r; ++j) in_k[j] = c[j].idx;
+  free(c);
+  /* insertion order of indices: a plain sort of r integers */
+  for (int64_t a = 1; a < r; ++a) {
+    int64_t v = in_k[a], b = a - 1;
+    while (b >= 0 && in_k[b] > v) {
+      in_k[b + 1] = in_k[b];
+      --b;
+    }
+    in_k[b + 1] = v;
+  }
+  top2_t t;
+  top2_init(&t);
+  for (int64_t j = 0; j < r; ++j) {
+    int64_t i = in_k[j];
+    double x = oracle_load(row, dtype, i);
+    double s = x == INFINITY ? INFINITY
+                             : x / T + oracle_gumbel(oracle_uniform(
+                                           oracle_stream_word(seed, row_id, (uint64_t)i, offset)));
+    top2_push(&t, i, s);
+  }
+  free(in_k);
+  if (gap) *gap = top2_gap(&t);
+  return t.idx;
+}
+
+void oracle_filtered_gumbel_argmax(const void* logits, int dtype, int64_t B, int64_t V,
+                                   int64_t ld, const float* temperature, const uint64_t* seed,
+                                   const uint64_t* offset, const int32_t* top_k,
+                                   const float* top_p, int64_t* out_idx, double* out_gap,
+                                   double* out_edge) {
+  for (int64_t b = 0; b < B; ++b) {
+    const char* row = (const char*)logits + b * ld * elt_size(dtype);
+    out_idx[b] = oracle_filtered_sample_row(
+        row, dtype, V, temperature[b], seed[b], (uint32_t)b, offset[b], top_k ? top_k[b] : 0,
+        top_p ? top_p[b] : 1.0f, out_gap ? &out_gap[b] : NULL, out_edge ? &out_edge[b] : NULL);
+  }
+}
+
+/* Many decode steps of one filtered batch (offset base_offset + k for every
+ * row at step k); out_idx is [steps][B]. */
+void oracle_filtered_steps(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                           const float* temperature, const uint64_t* seed, uint64_t base_offset,
+                           int64_t steps, const int32_t* top_k, const float* top_p,
+                           int64_t* out_idx) {
+  for (int64_t k = 0; k < steps; ++k)
+    for (int64_t b = 0; b < B; ++b) {
+      const char* row = (const char*)logits + b * ld * elt_size(dtype);
+      out_idx[k * B + b] = oracle_filtered_sample_row(
+          row, dtype, V, temperature[b], seed[b], (uint32_t)b, base_offset + (uint64_t)k,
+          top_k ? top_k[b] : 0, top_p ? top_p[b] : 1.0f, NULL, NULL);
+    }
 }
 
 /* ----------------------------------------------------------------------------

@@ -95,3 +95,43 @@ def rows_at_steps(kind: str, logits, dtype, T, S, steps, extra=None, row_ids=Non
     idx = np.array([r[0] for r in res], dtype=np.int64).reshape(len(steps), n)
     gap = np.array([r[1] for r in res], dtype=np.float64).reshape(len(steps), n)
     return idx, gap
+
+
+def _filtered_chunk(args):
+    import oracle
+
+    logits, dtype, temperature, seed, base, steps, top_k, top_p = args
+    return oracle.filtered_steps(logits, temperature, seed, base, steps, top_k=top_k,
+                                 top_p=top_p, dtype=dtype)
+
+
+def filtered_steps(logits, temperature, seed, base: int, steps: int, dtype: int, top_k=0,
+                   top_p=1.0):
+    """oracle.filtered_steps spread over worker processes by step range."""
+    n = max(1, min(steps, 4 * (os.cpu_count() or 1)))
+    edges = np.linspace(0, steps, n + 1).astype(np.int64)
+    jobs = [(logits, dtype, temperature, seed, base + int(a), int(b - a), top_k, top_p)
+            for a, b in zip(edges[:-1], edges[1:]) if b > a]
+    return np.concatenate(list(pool().map(_filtered_chunk, jobs)))
+
+
+def _filtered_row_job(args):
+    import oracle
+
+    row, dtype, T, seed, row_id, offset, k, p = args
+    return oracle.filtered_sample_row(row, T, seed, row_id, offset, top_k=k, top_p=p, dtype=dtype)
+
+
+def filtered_rows_at_steps(logits, dtype, T, S, steps, top_k, top_p, row_ids=None):
+    """Filtered oracle draws of the selected rows at every step in `steps`, one
+    (step, row) per task. -> (idx, gap, edge), each [len(steps), n]."""
+    B = logits.shape[0]
+    row_ids = np.arange(B) if row_ids is None else np.asarray(row_ids)
+    rows_c = {int(r): np.ascontiguousarray(logits[r]) for r in row_ids}
+    jobs = [(rows_c[int(r)], dtype, float(T[r]), int(S[r]), int(r), int(s), int(top_k[r]),
+             float(top_p[r])) for s in steps for r in row_ids]
+    res = list(pool().map(_filtered_row_job, jobs, chunksize=max(1, len(jobs) // 256)))
+    shape = (len(steps), len(row_ids))
+    return (np.array([r[0] for r in res], dtype=np.int64).reshape(shape),
+            np.array([r[1] for r in res], dtype=np.float64).reshape(shape),
+            np.array([r[2] for r in res], dtype=np.float64).reshape(shape))
