@@ -514,9 +514,11 @@ void oracle_categorical(const void* logits, int dtype, int64_t B, int64_t V, int
  * library sort of the candidates, the prefix, then the restricted argmax.
  * Temperature <= 0 or NaN: greedy argmax (the filters keep the top element).
  * Outputs: gap = the top-two score gap within K (as oracle_sample_row);
- * edge = how far the nucleus boundary is from moving by one element, relative
- * to S: min((cum_r - p S) / S, (p S - cum_{r-1}) / S) at r = r_p, or +inf when
- * the nucleus does not decide K (top_p inactive, or r_k < r_p).
+ * edge = how far top_p * S (relative to S) may move before the answer
+ * changes: down to the mass of the candidates before the winner (the winner
+ * leaves K; never for the first candidate, which K always keeps), or up to the mass before the first later candidate, within r_k,
+ * whose score beats the winner's (it joins K); +inf when the nucleus does
+ * not decide K (top_p inactive, or r_k < r_p).
  * ------------------------------------------------------------------------- */
 typedef struct {
   int64_t idx;
@@ -564,45 +566,63 @@ int64_t oracle_filtered_sample_row(const void* row, int dtype, int64_t V, float 
     double S = 0.0;
     for (int64_t j = 0; j < n; ++j)
       S += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
-    double cum = 0.0, before = 0.0;
+    double cum = 0.0;
     for (int64_t j = 0; j < n; ++j) {
-      before = cum;
       cum += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
       if (cum >= p * S) {
         r_p = j + 1;
         break;
       }
     }
-    if (edge && r_p <= r_k) *edge = fmin((cum - p * S) / S, (p * S - before) / S);
   }
   int64_t r = r_k < r_p ? r_k : r_p;
-  /* The restricted argmax, visiting K in index order so that only a strictly
-   * larger score replaces the best (lowest index on ties). */
-  int64_t* in_k = (int64_t*)malloc((size_t)r * sizeof(int64_t));
-  for (int64_t j = 0; j < r; ++j) in_k[j] = c[j].idx;
-  free(c);
-  /* insertion order of indices: a plain sort of r integers */
-  for (int64_t a = 1; a < r; ++a) {
-    int64_t v = in_k[a], b = a - 1;
-    while (b >= 0 && in_k[b] > v) {
-      in_k[b + 1] = in_k[b];
-      --b;
+  /* Scores of the candidates in order, as far as the answer needs them: K,
+   * and, when the nucleus decides K and the edge is wanted, the candidates a
+   * larger top_p could add (up to r_k). */
+  int nucleus = p > 0.0 && p < 1.0 && r_p <= r_k;
+  int64_t limit = (edge && nucleus) ? r_k : r; /* >= r >= 1 */
+  double* sc = (double*)malloc((size_t)limit * sizeof(double));
+  for (int64_t j = 0; j < limit; ++j) {
+    double x = c[j].x;
+    sc[j] = x == INFINITY ? INFINITY
+                          : x / T + oracle_gumbel(oracle_uniform(oracle_stream_word(
+                                        seed, row_id, (uint64_t)c[j].idx, offset)));
+  }
+  /* The argmax over K (larger score, then lower index) and the top-two gap. */
+  int64_t best = 0;
+  double s1 = limit > 0 ? sc[0] : -INFINITY, s2 = -INFINITY;
+  for (int64_t j = 1; j < r; ++j) {
+    if (sc[j] > s1 || (sc[j] == s1 && c[j].idx < c[best].idx)) {
+      s2 = s1;
+      s1 = sc[j];
+      best = j;
+    } else if (sc[j] > s2) {
+      s2 = sc[j];
     }
-    in_k[b + 1] = v;
   }
-  top2_t t;
-  top2_init(&t);
-  for (int64_t j = 0; j < r; ++j) {
-    int64_t i = in_k[j];
-    double x = oracle_load(row, dtype, i);
-    double s = x == INFINITY ? INFINITY
-                             : x / T + oracle_gumbel(oracle_uniform(
-                                           oracle_stream_word(seed, row_id, (uint64_t)i, offset)));
-    top2_push(&t, i, s);
+  if (gap) *gap = (r < 2 || s2 == -INFINITY) ? INFINITY : (s1 == s2 ? 0.0 : s1 - s2);
+  if (edge && nucleus) {
+    /* How far top_p * S may move before the answer changes: down to the
+     * mass before the winner (it leaves K), or up to the mass before the
+     * first later candidate that would beat it (it joins K). */
+    double S = 0.0, cum = 0.0, before_best = 0.0, e = INFINITY;
+    for (int64_t j = 0; j < n; ++j)
+      S += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
+    for (int64_t j = 0; j < limit; ++j) {
+      if (j == best) before_best = cum;
+      if (j >= r && (sc[j] > s1 || (sc[j] == s1 && c[j].idx < c[best].idx))) {
+        e = (cum - p * S) / S;
+        break;
+      }
+      cum += n_inf ? (c[j].x == INFINITY ? 1.0 : 0.0) : exp((c[j].x - M) / T);
+    }
+    /* the first candidate never leaves K (every filter keeps it) */
+    *edge = best > 0 ? fmin(e, (p * S - before_best) / S) : e;
   }
-  free(in_k);
-  if (gap) *gap = top2_gap(&t);
-  return t.idx;
+  int64_t ans = c[best].idx;
+  free(sc);
+  free(c);
+  return ans;
 }
 
 void oracle_filtered_gumbel_argmax(const void* logits, int dtype, int64_t B, int64_t V,

@@ -132,10 +132,13 @@ def test_plus_inf_rows_and_empty_rows():
 
 
 def test_edge_margin_at_an_exact_boundary():
-    """Two equal logits carry half the mass each: top_p = 0.5 is reached exactly
-    by the first, so the nucleus boundary sits on the edge (margin 0); top_p =
-    0.75 has both cumulative masses a quarter away."""
+    """Two equal logits carry half the mass each; with the second one scoring
+    higher, top_p = 0.5 keeps only the first and sits exactly where the second
+    would join and win (margin 0); top_p = 0.75 keeps both and the winner would
+    leave K only below 0.5 (margin 0.25)."""
     x = np.array([0.0, 0.0], np.float32)
+    s = _scores(x, 1.0, 1, 0, 0)
+    assert s[1] > s[0]  # this stream's second element wins the pair
     _, _, e = oracle.filtered_sample_row(x, 1.0, 1, 0, 0, top_p=0.5)
     assert e == 0.0
     _, _, e = oracle.filtered_sample_row(x, 1.0, 1, 0, 0, top_p=0.75)
@@ -144,6 +147,50 @@ def test_edge_margin_at_an_exact_boundary():
     x = np.zeros(10, np.float32)
     _, _, e = oracle.filtered_sample_row(x, 1.0, 1, 0, 0, top_k=2, top_p=0.9)
     assert e == np.inf
+
+
+def test_edge_margin_brute_force():
+    """The margin is the distance (as a share of the row's mass) from top_p to
+    the nearest cut of the ordered candidates whose prefix has a different
+    Gumbel-max, found here by trying every prefix length up to top_k."""
+    rng = np.random.default_rng(13)
+    checked = 0
+    for k in range(300):
+        V = int(rng.integers(2, 60))
+        x = (rng.standard_normal(V) * rng.choice([0.3, 1.0, 3.0])).astype(np.float32)
+        x[rng.random(V) < 0.1] = -np.inf
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        top_p = float(np.float32(rng.uniform(0.05, 0.98)))
+        top_k = int(rng.choice([0, 3, 10, 40]))
+        idx, _, e = oracle.filtered_sample_row(x, T, 21, 3, k, top_k=top_k, top_p=top_p)
+        xd = x.astype(np.float64)
+        cand = np.flatnonzero(~np.isneginf(xd))
+        if cand.size == 0:
+            continue
+        order = cand[np.lexsort((cand, -xd[cand]))]
+        mass = np.exp((xd[order] - xd[order].max()) / np.float64(np.float32(T)))
+        S = mass.sum()
+        cum = np.concatenate([[0.0], np.cumsum(mass)])  # cum[r] = mass of the first r
+        n = order.size
+        r_k = top_k if 1 <= top_k < n else n
+        r_p = int(np.argmax(cum[1:] >= top_p * S)) + 1
+        if r_k < r_p:
+            assert e == np.inf
+            continue
+        s = _scores(x, T, 21, 3, k)[order]
+
+        def winner(r):
+            sk = s[:r]
+            return int(order[:r][sk == sk.max()].min())
+
+        assert winner(r_p) == idx
+        margins = [np.inf]
+        for r in range(1, r_k + 1):
+            if winner(r) != idx:
+                margins.append((cum[r - 1] - top_p * S) / S if r > r_p else (top_p * S - cum[r]) / S)
+        assert e == pytest.approx(min(margins), rel=1e-9, abs=1e-12), (k, e, min(margins))
+        checked += 1
+    assert checked > 200
 
 
 N_DRAWS = 1_000_000
