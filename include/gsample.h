@@ -120,6 +120,40 @@ gsample_status gsample_gumbel_argmax(const void* logits, gsample_dtype dtype, in
                                      int64_t* out_idx, void* workspace,
                                      gsample_stream_t stream);
 
+/* Top-k / top-p sampling on the Gumbel path, the follow-up "Softmax-free GPU
+ * sampling" (Background) names as rejection-based top-k/top-p. Per row b the
+ * filter set K is the first r candidates (logits that are neither NaN nor
+ * -inf) in the order (logit descending, index ascending), where r is the
+ * smaller of
+ *   - top_k[b], when top_k[b] >= 1 (else no limit), and
+ *   - the smallest prefix whose softmax(x / T) mass reaches top_p[b] * (row
+ *     mass), when top_p[b] < 1 (top_p[b] <= 0 keeps the first candidate only;
+ *     top_p[b] >= 1 or NaN: no limit);
+ * and out_idx[b] is the Gumbel-max over K with the same noise as
+ * gsample_gumbel_argmax: argmax over i in K of x_i / T + g_i, lowest index on
+ * ties. It is an exact draw of softmax(x / T) restricted to K.
+ *   - Rejection: the unfiltered draw (gsample_gumbel_argmax) is a proposal; a
+ *     second pass over each filtered row keeps it when it lies in K (it is
+ *     then the argmax over K); rejected rows are resolved exactly by a radix
+ *     select of K's last element and the Gumbel-max over K. Three launches on
+ *     `stream`, no host synchronisation.
+ *   - top_k and top_p are device arrays of B entries (int32, float); either
+ *     may be NULL (that filter off for every row). Both NULL: the same as
+ *     gsample_gumbel_argmax.
+ *   - Rows with temperature <= 0 or NaN are greedy (K always holds the top
+ *     element). A row with a +inf logit returns its lowest +inf index.
+ *   - The nucleus masses are binary32 sums on the GPU: a row whose top_p lands
+ *     within ~1e-5 of the row mass from a prefix boundary may take one element
+ *     more or less than an exact computation would.
+ *   - Workspace, layout, validation and asynchrony as gsample_gumbel_argmax; a
+ *     misaligned top_k/top_p (4 bytes) returns GSAMPLE_ERR_INVALID_ARG. */
+gsample_status gsample_filtered_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                              int64_t V, int64_t ld, const float* temperature,
+                                              const uint64_t* seed, const uint64_t* offset,
+                                              const int32_t* top_k, const float* top_p,
+                                              int64_t* out_idx, void* workspace,
+                                              gsample_stream_t stream);
+
 /* HLG tone curve on the row's log-probs, then Gumbel-max ("HLG sampling",
  * sections "The transfer function", "The pivot", "Temperature semantics"):
  *     score_i = g(l_i - mu) / T + g_i,

@@ -240,3 +240,23 @@ def test_hlg_score_debug_validation():
     assert L.gsample_debug_hlg_score(None, FAKE, 4, ctypes.byref(hp), 1.0, 1.0, FAKE, st) == \
         gs.ERR_INVALID_ARG
     assert L.gsample_debug_hlg_score(FAKE, FAKE, 0, ctypes.byref(hp), 1.0, 1.0, FAKE, st) == gs.OK
+
+
+def test_filtered_entry_validation():
+    L = gs.lib()
+
+    def call(B=4, logits=FAKE, T=FAKE, k=FAKE, p=FAKE, out=FAKE, ws=FAKE):
+        return L.gsample_filtered_gumbel_argmax(logits, gs.F32, B, 100, 100, T, FAKE, FAKE, k, p,
+                                                out, ws, None)
+
+    assert call(B=0) == gs.OK
+    assert call(logits=None) == gs.ERR_INVALID_ARG
+    assert call(T=None) == gs.ERR_INVALID_ARG
+    assert call(k=FAKE + 2) == gs.ERR_INVALID_ARG       # int32 array, 4-byte aligned
+    assert call(p=FAKE + 1) == gs.ERR_INVALID_ARG
+    assert call(out=FAKE + 4) == gs.ERR_INVALID_ARG
+    assert call(ws=None) == gs.ERR_INVALID_ARG
+    assert call(ws=FAKE + 8) == gs.ERR_WORKSPACE
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call(k=None, p=None) == gs.ERR_CUDA

@@ -24,7 +24,7 @@ __all__ = [
     "GSampleError", "HlgParams", "PIVOT_TOP", "PIVOT_ENTROPY", "F32", "BF16", "F16",
     "lib", "library_path", "workspace_bytes", "workspace_init", "new_workspace", "argmax",
     "gumbel_argmax", "hlg_gumbel_argmax", "hlg_gumbel_argmax_rows", "hlg_rows_tensor",
-    "categorical", "status_string",
+    "categorical", "filtered_gumbel_argmax", "status_string",
 ]
 
 F32, BF16, F16 = 0, 1, 2
@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
                                                     _vp, _vp]),
             "gsample_gumbel_argmax_host": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                   _vp, _vp, _vp]),
+            "gsample_filtered_gumbel_argmax": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                      _vp, _vp, _vp, _vp, _vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -244,6 +246,28 @@ def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, c
         st = L.gsample_gumbel_argmax(logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(),
                                      O.data_ptr(), out.data_ptr(), ws.data_ptr(), _stream_ptr(dev))
     _check(st, "gsample_gumbel_argmax")
+    return out
+
+
+def filtered_gumbel_argmax(logits, temperature, seed, offset, top_k=None, top_p=None, out=None,
+                           workspace=None):
+    """Top-k / top-p Gumbel-max sample per row (gsample_filtered_gumbel_argmax):
+    the Gumbel-max over the row's filter set K (the top_k largest logits and/or
+    the smallest prefix whose softmax mass reaches top_p). top_k (int32) and
+    top_p (float32) are per-row tensors, scalars, or None (filter off)."""
+    torch = _torch()
+    dt, B, V, ld, out, ws = _prepare(logits, out, workspace)
+    dev = logits.device
+    T = _row_tensor(temperature, B, torch.float32, dev, "temperature")
+    S = _row_tensor(seed, B, torch.int64, dev, "seed")
+    O = _row_tensor(offset, B, torch.int64, dev, "offset")
+    K = None if top_k is None else _row_tensor(top_k, B, torch.int32, dev, "top_k")
+    P = None if top_p is None else _row_tensor(top_p, B, torch.float32, dev, "top_p")
+    st = lib().gsample_filtered_gumbel_argmax(
+        logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(), O.data_ptr(),
+        None if K is None else K.data_ptr(), None if P is None else P.data_ptr(), out.data_ptr(),
+        ws.data_ptr(), _stream_ptr(dev))
+    _check(st, "gsample_filtered_gumbel_argmax")
     return out
 
 

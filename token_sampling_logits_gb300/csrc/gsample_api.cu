@@ -469,6 +469,45 @@ gsample_status gsample_gumbel_argmax(const void* logits, gsample_dtype dtype, in
                     (cudaStream_t)stream);
 }
 
+gsample_status gsample_filtered_gumbel_argmax(const void* logits, gsample_dtype dtype, int64_t B,
+                                              int64_t V, int64_t ld, const float* temperature,
+                                              const uint64_t* seed, const uint64_t* offset,
+                                              const int32_t* top_k, const float* top_p,
+                                              int64_t* out_idx, void* workspace,
+                                              gsample_stream_t stream) {
+  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)top_k % 4 || (uintptr_t)top_p % 4) return GSAMPLE_ERR_INVALID_ARG;
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (st != GSAMPLE_OK || B == 0) return st;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  // The proposals: the plain sampler over every row.
+  st = run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
+                  (cudaStream_t)stream);
+  if (st != GSAMPLE_OK || (!top_k && !top_p)) return st;
+  const bool vec = vec_path(logits, dtype, ld);
+  const int epu = gsample::units_elems((int)dtype, vec);
+  gsample::FilterParams fp;
+  fp.logits = static_cast<const char*>(logits);
+  fp.ld_bytes = ld * elt_bytes(dtype);
+  fp.B = B;
+  fp.V = (int32_t)V;
+  fp.units_per_row = (int32_t)((V + epu - 1) / epu);
+  fp.temperature = temperature;
+  fp.seed = seed;
+  fp.offset = offset;
+  fp.top_k = top_k;
+  fp.top_p = top_p;
+  fp.out_idx = out_idx;
+  fp.ws = static_cast<WsRow*>(workspace);
+  if (gsample::launch_filter(fp, (int)dtype, vec, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
 gsample_status gsample_gumbel_argmax_host(const void* logits, gsample_dtype dtype, int64_t B,
                                           int64_t V, int64_t ld, const float* temperature,
                                           const uint64_t* seed, const uint64_t* offset,

@@ -81,6 +81,25 @@ struct RowClusterParams {
   int64_t* out_idx;
 };
 
+// Top-k / top-p on the Gumbel path, after the plain sampler has written its
+// proposals into out_idx: one CTA per row checks the proposal, then one CTA
+// per rejected row (flagged in ws[b].hint) resolves it exactly.
+struct FilterParams {
+  const char* logits;
+  int64_t ld_bytes;
+  int64_t B;
+  int32_t V;
+  int32_t units_per_row;
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  const int32_t* top_k;  // nullptr: no top-k
+  const float* top_p;    // nullptr: no top-p
+  int64_t* out_idx;
+  WsRow* ws;
+};
+cudaError_t launch_filter(const FilterParams& p, int dtype, bool vec, cudaStream_t stream);
+
 // Elements per unit for a dtype code (0 f32, 1 bf16, 2 f16) and load path.
 inline int units_elems(int dtype, bool vec) { return vec ? (dtype == 0 ? 4 : 8) : 4; }
 
