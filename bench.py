@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--quick", action="store_true",
                     help="headline timing only (no CPU baseline, e2e, clocks or table); for "
                          "profiler runs")
-    ap.add_argument("--workload", choices=["throughput", "sweep", "hlg", "mixed_greedy"],
+    ap.add_argument("--workload", choices=["throughput", "sweep", "hlg", "mixed_greedy",
+                                           "filtered"],
                     default="throughput",
                     help="with --quick: time this workload instead of the headline (sweep takes "
                          "--batch and --vocab); prints a short line, for profiler runs")
@@ -314,7 +315,7 @@ class Runner:
     captured CUDA graphs (see the module docstring for the buffer pool)."""
 
     def __init__(self, batch: W.Batch, hlg=None, min_pool_bytes: int = 0, ring: int = 1000,
-                 categorical: bool = False):
+                 categorical: bool = False, filters=None):
         import ctypes
 
         import torch
@@ -342,6 +343,11 @@ class Runner:
         self.dt, _, _, self.ld = gs._logits_args(self.pool[0])
         self.hp = hlg.to_c() if hlg is not None else None
         self.categorical = categorical
+        # (top_k int32[B], top_p float32[B]) for gsample_filtered_gumbel_argmax
+        self.filters = None
+        if filters is not None:
+            self.filters = (torch.from_numpy(np.asarray(filters[0], np.int32)).cuda(),
+                            torch.from_numpy(np.asarray(filters[1], np.float32)).cuda())
         self.graphs = {}
         self.launches = 0
 
@@ -356,6 +362,12 @@ class Runner:
                                            self.T.data_ptr(), self.S.data_ptr(),
                                            self.offs.data_ptr() + 8 * B * k,
                                            self.out.data_ptr() + 8 * B * k, st)
+            elif self.filters is not None:
+                rc = L.gsample_filtered_gumbel_argmax(
+                    x.data_ptr(), self.dt, B, self.V, self.ld, self.T.data_ptr(),
+                    self.S.data_ptr(), self.offs.data_ptr() + 8 * B * k,
+                    self.filters[0].data_ptr(), self.filters[1].data_ptr(),
+                    self.out.data_ptr() + 8 * B * k, self.ws.data_ptr(), st)
             elif self.hp is None:
                 rc = L.gsample_gumbel_argmax(x.data_ptr(), self.dt, B, self.V, self.ld,
                                              self.T.data_ptr(), self.S.data_ptr(),
@@ -574,8 +586,11 @@ def extra_table(dist: Dist, l2: int):
                       pivot_offset=p["c"])
     cases.append(("hlg", W.hlg(), hp))
     cases.append(("mixed_greedy", W.mixed_greedy(), None))
-    def timed(b, h=None, categorical=False, single=False):
-        r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500, categorical=categorical)
+    # top-k / top-p on the headline batch: top_k = 50 and top_p = 0.9 on every row
+    cases.append(("filtered", W.throughput(HEADLINE_B), None))
+    def timed(b, h=None, categorical=False, single=False, filters=None):
+        r = Runner(b, hlg=h, min_pool_bytes=4 * l2, ring=500, categorical=categorical,
+                   filters=filters)
         steps = r.ring * max(1, (2000 if b.B * b.V < 50_000_000 else 500) // r.ring)
         ms, _ = time_steps(r, steps, 50, dist)
         one = r.single_launch_us() if single else None
@@ -583,13 +598,18 @@ def extra_table(dist: Dist, l2: int):
         return (ms * 1000 / steps, one) if single else ms * 1000 / steps
 
     for kind, b, h in cases:
-        us, one = timed(b, h, single=True)
+        filt = ((np.full(b.B, 50, np.int32), np.full(b.B, 0.9, np.float32))
+                if kind == "filtered" else None)
+        us, one = timed(b, h, single=True, filters=filt) if filt is None else \
+            (timed(b, h, filters=filt), None)
         nbytes = b.B * (b.V * (4 if b.dtype == W.F32 else 2) + PER_ROW_PARAM_BYTES)
         row = {"workload": kind, "B": b.B, "V": b.V, "dtype": W.DTYPE_NAMES[b.dtype],
                "us_per_step": round(us, 3), "rows_per_s": round(b.B / us * 1e6, 1),
                "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4),
-               "single_launch_us": round(one, 3)}
+               "single_launch_us": round(one, 3) if one is not None else None}
+        if kind == "filtered":
+            row["filters"] = "top_k=50, top_p=0.9 on every row (three launches per step)"
         if kind == "sweep":
             # The issue's comparison: the categorical (softmax + inverse-CDF)
             # path against Gumbel-max on the same V x B grid.
@@ -618,14 +638,18 @@ def run_case(args):
                           pivot_offset=p["c"])
     elif args.workload == "mixed_greedy":
         b = W.mixed_greedy()
+    elif args.workload == "filtered":
+        b = W.throughput(args.batch)
     else:
         b = W.throughput(args.batch)
     if hp is not None and args.categorical:
         raise SystemExit("--categorical has no HLG form")
     props = torch.cuda.get_device_properties(0)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    filt = ((np.full(b.B, 50, np.int32), np.full(b.B, 0.9, np.float32))
+            if args.workload == "filtered" else None)
     r = Runner(b, hlg=hp, min_pool_bytes=4 * l2, ring=max(1, args.steps),
-               categorical=args.categorical)
+               categorical=args.categorical, filters=filt)
     ms, _ = time_steps(r, args.steps, max(3, args.warmup), Dist(1))
     print(json.dumps({"workload": args.workload, "B": b.B, "V": b.V,
                       "dtype": W.DTYPE_NAMES[b.dtype], "categorical": args.categorical,
