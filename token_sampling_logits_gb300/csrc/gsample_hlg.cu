@@ -55,19 +55,6 @@ __device__ __forceinline__ Moments merge(Moments a, Moments b) {
   return Moments{M, a.S * fa + b.S * fb, a.W * fa + b.W * fb};
 }
 
-__device__ __forceinline__ void push(Moments& mo, float x) {
-  if (x > mo.M) {
-    const float f = mo.M == -INFINITY ? 0.0f : __expf(mo.M - x);
-    mo.S = mo.S * f + 1.0f;
-    mo.W = mo.W * f + x;
-    mo.M = x;
-  } else {
-    const float e = __expf(x - mo.M);
-    mo.S += e;
-    mo.W += e * x;
-  }
-}
-
 // The tone curve in binary32 ("The transfer function"). rbt, rbh are 1/beta.
 struct Curve {
   float m, w, bt, bh, rbt, rbh;

@@ -95,11 +95,6 @@ struct Cfg {
   static constexpr size_t kSmem = (size_t)kWarps * kWarpBytes;
 };
 
-template <int DT>
-__device__ __forceinline__ float half_to_f32(uint32_t h) {
-  return DT == 1 ? bf16_bits_to_f32(h) : f16_bits_to_f32(h);
-}
-
 // Element e (0 <= e < kEPU) of a unit.
 template <int DT, bool VEC>
 __device__ __forceinline__ float unit_elt(const uint4& r, int e) {
@@ -154,46 +149,6 @@ __device__ __forceinline__ uint4 load_unit_sync(const char* row, int32_t u, int3
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// ---------------------------------------------------------------------------
-// Shared-memory and cp.async primitives.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "l"(pol)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -733,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, GSAMPLE_MIN_CTAS_PER_SM) sample_kern
   const uint32_t ring = smem_addr(wbase);
   const uint64_t pol = evict_first_policy();
 
-  const int64_t U = p.total_units, NU = p.units_per_row, NW = p.warps;
+  const int64_t NU = p.units_per_row, NW = p.warps;
   const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
   if (gw >= NW) return;
   const int64_t u_begin = split_point<VEC>(p, gw), u_end = split_point<VEC>(p, gw + 1);

@@ -1,6 +1,7 @@
 // Helpers shared by the kernels that hold a row slice in shared memory (the
-// HLG sampler and the categorical baseline): unit shapes, element decoding,
-// unit loads with -inf padding, and the cp.async / shared-memory primitives.
+// HLG sampler, the categorical baseline, the small-batch sampler and the
+// filtered path): unit shapes, element decoding and unit loads with -inf
+// padding. The cp.async / shared-memory primitives live in gsample_device.cuh.
 #pragma once
 
 #include <cstdint>
@@ -16,11 +17,6 @@ struct HCfg {
   static constexpr int kGPU = kEPU / 4;
   static constexpr bool kF32Bits = DT == 0 || !VEC;
 };
-
-template <int DT>
-__device__ __forceinline__ float half_to_f32(uint32_t h) {
-  return DT == 1 ? bf16_bits_to_f32(h) : f16_bits_to_f32(h);
-}
 
 template <int DT, bool VEC>
 __device__ __forceinline__ float elt(const uint4& r, int e) {
@@ -63,26 +59,6 @@ __device__ __forceinline__ uint4 load_unit(const char* row, int32_t u, int32_t V
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "l"(pol)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
 }
 
 }  // namespace slice
