@@ -229,10 +229,12 @@ def kernel_source_hash(names=SAMPLE_KERNEL_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def profile_figure(profile_name: str, key: str, workload_rows: int):
+def profile_figure(profile_name: str, key: str, workload_rows: int,
+                   rows_key: str = "captured_rows"):
     """A per-launch figure recorded under profiles/ (`key: value`, with the
-    kernel-source hash and the rows of the captured launch), scaled to the
-    benchmark's batch; None when the kernel sources changed since."""
+    kernel-source hash and the rows of the launch it was taken on, under
+    rows_key), scaled to the benchmark's batch; None when the kernel sources
+    changed since."""
     path = os.path.join(ROOT, "profiles", profile_name)
     try:
         text = open(path).read()
@@ -240,7 +242,7 @@ def profile_figure(profile_name: str, key: str, workload_rows: int):
         return None
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_val = re.search(r"%s:\s*([0-9.eE+]+)" % re.escape(key), text)
-    m_rows = re.search(r"captured_rows:\s*(\d+)", text)
+    m_rows = re.search(r"%s:\s*(\d+)" % re.escape(rows_key), text)
     if not (m_hash and m_val and m_rows) or m_hash.group(1) != kernel_source_hash():
         return None
     return float(m_val.group(1)) * workload_rows / int(m_rows.group(1))
@@ -706,7 +708,7 @@ def run_ours(args, dist: Dist):
     # count recorded under profiles/ is used while the kernel sources match.
     alg_blocks = batch.B * ((batch.V + 3) // 4)
     computed = profile_figure("sample_kernel_bf16_throughput.md", "philox_blocks_per_launch",
-                              batch.B)
+                              batch.B, rows_key="philox_count_rows")
     ppeak, ppeak_kind = philox_peak() if not args.quick else (None, None)
     hbm_view = {"achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind + " (copy bandwidth)",
@@ -857,7 +859,7 @@ def run_count_blocks(args):
             raise RuntimeError("gsample_debug_blocks_computed: " + gs.status_string(rc))
         res["T=%g" % T] = cnt.value / n
     alg = base.B * ((base.V + 3) // 4)
-    print(json.dumps({"kernel_source_hash": kernel_source_hash(), "captured_rows": base.B,
+    print(json.dumps({"kernel_source_hash": kernel_source_hash(), "philox_count_rows": base.B,
                       "algorithmic_blocks_per_launch": alg,
                       "philox_blocks_per_launch": res,
                       "share_of_algorithmic": {k: round(v / alg, 4) for k, v in res.items()}}),

@@ -91,10 +91,13 @@ def test_recorded_block_count_is_scaled_and_nulled_on_source_change(tmp_path, mo
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1000\n"
-                               "philox_blocks_per_launch: 640\ncaptured_rows: 10\n" % h)
+                               "philox_blocks_per_launch: 640\ncaptured_rows: 10\n"
+                               "philox_count_rows: 5\n" % h)
     monkeypatch.setattr(b, "ROOT", str(tmp_path))
     monkeypatch.setattr(b, "kernel_source_hash", lambda: h)
     assert b.profile_figure("p.md", "philox_blocks_per_launch", 20) == pytest.approx(1280.0)
+    assert b.profile_figure("p.md", "philox_blocks_per_launch", 20,
+                            rows_key="philox_count_rows") == pytest.approx(2560.0)
     assert b.profile_figure("p.md", "not_recorded", 20) is None
     monkeypatch.setattr(b, "kernel_source_hash", lambda: "0" * 16)
     assert b.profile_figure("p.md", "philox_blocks_per_launch", 20) is None
