@@ -70,6 +70,17 @@ gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dt
                                             int64_t* out_idx, int32_t cluster,
                                             gsample_stream_t stream);
 
+/* gsample_filtered_gumbel_argmax with an explicit cluster size for the
+ * filter (CTAs per row, 1..16, at most what the device co-schedules;
+ * 0 = the library's choice). A CTA whose slice exceeds the filter's shared
+ * memory re-reads it from global memory in every phase. */
+gsample_status gsample_debug_filtered_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                         int64_t V, int64_t ld, const float* temperature,
+                                         const uint64_t* seed, const uint64_t* offset,
+                                         const int32_t* top_k, const float* top_p,
+                                         int64_t* out_idx, void* workspace, int32_t cluster,
+                                         gsample_stream_t stream);
+
 /* Philox4x32-10 throughput of the kernels' block code alone (Salmon et al.,
  * SC'11; the row-folded first two rounds and four blocks per thread side by
  * side, as in the sampler). One CTA per SM of warps_per_sm warps (1..32); each

@@ -24,20 +24,21 @@ torch = pytest.importorskip("torch")
 NEAR_EDGE = 1e-5
 
 
-def _gpu(batch, K, P, x=None, ws=None):
+def _gpu(batch, K, P, x=None, ws=None, cluster=0):
     x = to_device(batch.logits, batch.dtype) if x is None else x
     T, S, O = rows_to_device(batch)
     Kt = None if K is None else torch.from_numpy(np.asarray(K, np.int32)).cuda()
     Pt = None if P is None else torch.from_numpy(np.asarray(P, np.float32)).cuda()
-    out = gs.filtered_gumbel_argmax(x, T, S, O, top_k=Kt, top_p=Pt, workspace=ws)
+    out = gs.filtered_gumbel_argmax(x, T, S, O, top_k=Kt, top_p=Pt, workspace=ws,
+                                    cluster=cluster)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
 
-def _check(b, K, P, tally, where, x=None):
+def _check(b, K, P, tally, where, x=None, cluster=0):
     Kf = np.zeros(b.B, np.int32) if K is None else np.asarray(K, np.int32)
     Pf = np.ones(b.B, np.float32) if P is None else np.asarray(P, np.float32)
-    got = _gpu(b, K, P, x=x)
+    got = _gpu(b, K, P, x=x, cluster=cluster)
     ref, gap, edge = _oracle(b, Kf, Pf)
     greedy = ~(b.temperature > 0)
     # rows on a nucleus edge are exempted like near-ties (gap set to 0) and counted
@@ -78,6 +79,52 @@ def test_filtered_shapes(dtype, B, V):
         _check(b, K, None, t, "top-k only")
         _check(b, None, P, t, "top-p only")
     register("6 filtered (edge cases)", t, assert_bound=False)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16, W.F16])
+@pytest.mark.parametrize("cluster", [1, 3, 16])
+def test_forced_cluster_sizes(dtype, cluster):
+    """The filter at forced cluster sizes: one CTA per row (slices of 240-480 KB
+    at V = 120001, re-read from global memory in every phase), an odd size,
+    and sixteen CTAs (some of them with an empty slice on the small rows).
+    Logits on a coarse grid put many entries on K's last key, so the tie rule
+    (lower index first) splits a tie group across CTA slices."""
+    t = Tally()
+    for B, V in ((6, 20000), (3, 37), (4, 120001)):
+        rng = np.random.default_rng([cluster, B, V, dtype])
+        x = (rng.standard_normal((B, V)) * 2.0).astype(np.float32)
+        x[::2] = np.round(x[::2] * 2.0) / 2.0  # coarse grid: large tie groups
+        x[rng.random((B, V)) < 0.01] = -np.inf
+        x[rng.random((B, V)) < 0.005] = np.nan
+        T = rng.uniform(0.5, 2.0, B).astype(np.float32)
+        b = W.Batch("cluster", W.encode(x, dtype), dtype, T, W.splitmix64(cluster, B),
+                    np.full(B, 3, np.uint64))
+        K = rng.choice([1, 2, 7, 100, 3000], B).astype(np.int32)
+        P = rng.choice([1.0, 0.3, 0.8, 0.95], B).astype(np.float32)
+        for step in range(3):
+            bs = b.at_step(step)
+            _check(bs, K, P, t, "cluster=%d B=%d V=%d" % (cluster, B, V), cluster=cluster)
+            _check(bs, K, None, t, "cluster=%d top-k" % cluster, cluster=cluster)
+            _check(bs, None, P, t, "cluster=%d top-p" % cluster, cluster=cluster)
+    register("6 filtered (edge cases)", t, assert_bound=False)
+
+
+def test_signed_zeros_tie():
+    """-0 and +0 are equal logits: the order puts the lower index first whatever
+    the sign, so top_k = 2 over a row topped by three zeros keeps the first two."""
+    B, V = 4, 3000
+    x = np.full((B, V), -5.0, np.float32)
+    x[:, [100, 1700, 2900]] = [[-0.0, 0.0, -0.0], [0.0, -0.0, 0.0], [-0.0, -0.0, 0.0],
+                               [0.0, 0.0, -0.0]]
+    b = W.Batch("zeros", x, W.F32, np.full(B, 0.25, np.float32), W.splitmix64(4, B),
+                np.zeros(B, np.uint64))
+    t = Tally()
+    for step in range(40):
+        bs = b.at_step(step)
+        got = _gpu(bs, np.full(B, 2, np.int32), None)
+        assert np.isin(got, [100, 1700]).all(), got
+        _check(bs, np.full(B, 2, np.int32), None, t, "zeros")
+        _check(bs, np.full(B, 2, np.int32), None, t, "zeros cluster 2", cluster=2)
 
 
 def test_rejections_and_acceptances_both_exercised():

@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
                                                   _vp, _vp, _vp]),
             "gsample_filtered_gumbel_argmax": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp,
                                                       _vp, _vp, _vp, _vp, _vp]),
+            "gsample_debug_filtered_ex": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                                 _vp, _vp, _vp, _i32, _vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -250,11 +252,12 @@ def gumbel_argmax(logits, temperature, seed, offset, out=None, workspace=None, c
 
 
 def filtered_gumbel_argmax(logits, temperature, seed, offset, top_k=None, top_p=None, out=None,
-                           workspace=None):
+                           workspace=None, cluster: int = 0):
     """Top-k / top-p Gumbel-max sample per row (gsample_filtered_gumbel_argmax):
     the Gumbel-max over the row's filter set K (the top_k largest logits and/or
     the smallest prefix whose softmax mass reaches top_p). top_k (int32) and
-    top_p (float32) are per-row tensors, scalars, or None (filter off)."""
+    top_p (float32) are per-row tensors, scalars, or None (filter off).
+    Diagnostics: cluster > 0 forces that many filter CTAs per row."""
     torch = _torch()
     dt, B, V, ld, out, ws = _prepare(logits, out, workspace)
     dev = logits.device
@@ -263,10 +266,13 @@ def filtered_gumbel_argmax(logits, temperature, seed, offset, top_k=None, top_p=
     O = _row_tensor(offset, B, torch.int64, dev, "offset")
     K = None if top_k is None else _row_tensor(top_k, B, torch.int32, dev, "top_k")
     P = None if top_p is None else _row_tensor(top_p, B, torch.float32, dev, "top_p")
-    st = lib().gsample_filtered_gumbel_argmax(
-        logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(), O.data_ptr(),
-        None if K is None else K.data_ptr(), None if P is None else P.data_ptr(), out.data_ptr(),
-        ws.data_ptr(), _stream_ptr(dev))
+    args = (logits.data_ptr(), dt, B, V, ld, T.data_ptr(), S.data_ptr(), O.data_ptr(),
+            None if K is None else K.data_ptr(), None if P is None else P.data_ptr(),
+            out.data_ptr(), ws.data_ptr())
+    if cluster:
+        st = lib().gsample_debug_filtered_ex(*args, cluster, _stream_ptr(dev))
+    else:
+        st = lib().gsample_filtered_gumbel_argmax(*args, _stream_ptr(dev))
     _check(st, "gsample_filtered_gumbel_argmax")
     return out
 

@@ -36,6 +36,7 @@ struct DeviceInfo {
   int hlg_cluster[6] = {0, 0, 0, 0, 0, 0};   // largest co-schedulable cluster, per (dtype, vec)
   int cat_cluster[6] = {0, 0, 0, 0, 0, 0};   // the same for the categorical baseline
   int rc_cluster[6] = {0, 0, 0, 0, 0, 0};    // the same for the small-batch sampler
+  int filt_cluster[6] = {0, 0, 0, 0, 0, 0};  // the same for the top-k / top-p filter
 };
 
 std::mutex g_mu;
@@ -86,6 +87,12 @@ gsample_status device_info(const DeviceInfo** out) {
             return GSAMPLE_ERR_CUDA;
           }
           d.rc_cluster[dt * 2 + v] = rc;
+          const int fc = gsample::filter_max_cluster(dt, v != 0);
+          if (fc <= 0) {
+            cudaGetLastError();
+            return GSAMPLE_ERR_CUDA;
+          }
+          d.filt_cluster[dt * 2 + v] = fc;
         }
     }
     d.ready = true;
@@ -158,6 +165,33 @@ int pick_cluster(void* (*kernel)(int, bool, bool, int*), int dtype, bool vec, in
     }
   }
   return best;
+}
+
+#ifndef GSAMPLE_FILT_SLICE_BYTES
+#define GSAMPLE_FILT_SLICE_BYTES 40960
+#endif
+
+// The filter's cluster size for B rows of nu units: the smallest power of two
+// (at most max_cluster) whose slices fit in GSAMPLE_FILT_SLICE_BYTES of shared
+// memory, so that several CTAs share an SM; then doubled while the whole batch
+// still runs in one wave and every CTA keeps a unit per thread.
+int pick_filter_cluster(int dtype, bool vec, int64_t B, int64_t nu, int max_cluster) {
+  const size_t limit = gsample::filter_smem_limit();
+  int c = 1;
+  while (c < max_cluster && (nu + c - 1) / c * 16 > GSAMPLE_FILT_SLICE_BYTES)
+    c = 2 * c < max_cluster ? 2 * c : max_cluster;
+  for (;;) {
+    const int c2 = 2 * c < max_cluster ? 2 * c : max_cluster;
+    if (c2 == c) break;
+    const int64_t upc = (nu + c2 - 1) / c2;
+    int threads = 0;
+    const size_t smem = (size_t)upc * 16;
+    const bool resident = smem <= limit;
+    void* fn = gsample::filter_kernel_fn(dtype, vec, resident, &threads);
+    if (upc < threads || B > active_clusters(fn, threads, c2, resident ? smem : 0)) break;
+    c = c2;
+  }
+  return c;
 }
 
 gsample_status check_common(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
@@ -413,6 +447,58 @@ gsample_status run_hlg(const void* logits, gsample_dtype dtype, int64_t B, int64
   return GSAMPLE_OK;
 }
 
+// The proposals (the plain sampler over every row), then the filter: one
+// cluster per row tests each proposal and resolves the rejected ones.
+gsample_status run_filtered(const void* logits, gsample_dtype dtype, int64_t B, int64_t V,
+                            int64_t ld, const float* temperature, const uint64_t* seed,
+                            const uint64_t* offset, const int32_t* top_k, const float* top_p,
+                            int64_t* out_idx, void* workspace, int32_t cluster_override,
+                            cudaStream_t stream) {
+  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
+  if ((uintptr_t)top_k % 4 || (uintptr_t)top_p % 4) return GSAMPLE_ERR_INVALID_ARG;
+  if (cluster_override < 0 || cluster_override > 16) return GSAMPLE_ERR_INVALID_ARG;
+  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
+  if (st != GSAMPLE_OK || B == 0) return st;
+  const DeviceInfo* d = nullptr;
+  st = device_info(&d);
+  if (st != GSAMPLE_OK) return st;
+  const bool vec = vec_path(logits, dtype, ld);
+  const int epu = gsample::units_elems((int)dtype, vec);
+  const int64_t nu = (V + epu - 1) / epu;
+  const int max_cluster = d->filt_cluster[(int)dtype * 2 + (vec ? 1 : 0)];
+  if (cluster_override > max_cluster) return GSAMPLE_ERR_INVALID_ARG;
+  if (B * (cluster_override > 0 ? cluster_override : max_cluster) > (int64_t)INT32_MAX)
+    return GSAMPLE_ERR_INVALID_ARG;  // grid size
+  st = run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
+                  stream);
+  if (st != GSAMPLE_OK || (!top_k && !top_p)) return st;
+  gsample::FilterParams fp;
+  fp.logits = static_cast<const char*>(logits);
+  fp.ld_bytes = ld * elt_bytes(dtype);
+  fp.B = B;
+  fp.V = (int32_t)V;
+  fp.units_per_row = (int32_t)nu;
+  fp.cluster = cluster_override > 0 ? cluster_override
+                                    : pick_filter_cluster((int)dtype, vec, B, nu, max_cluster);
+  fp.units_per_cta = (int32_t)((nu + fp.cluster - 1) / fp.cluster);
+  // 2^E with a row's V masses of at most 2^E each below 2^63: E = 40 up to
+  // V = 2^22, one less per doubling above.
+  int lg = 0;
+  while ((int64_t(1) << lg) < V) ++lg;
+  fp.mass_scale = std::ldexp(1.0f, lg <= 22 ? 40 : 62 - lg);
+  fp.temperature = temperature;
+  fp.seed = seed;
+  fp.offset = offset;
+  fp.top_k = top_k;
+  fp.top_p = top_p;
+  fp.out_idx = out_idx;
+  if (gsample::launch_filter(fp, (int)dtype, vec, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GSAMPLE_ERR_CUDA;
+  }
+  return GSAMPLE_OK;
+}
+
 }  // namespace
 
 namespace gsample {
@@ -475,37 +561,8 @@ gsample_status gsample_filtered_gumbel_argmax(const void* logits, gsample_dtype 
                                               const int32_t* top_k, const float* top_p,
                                               int64_t* out_idx, void* workspace,
                                               gsample_stream_t stream) {
-  if (B > 0 && (!temperature || !seed || !offset)) return GSAMPLE_ERR_INVALID_ARG;
-  if ((uintptr_t)top_k % 4 || (uintptr_t)top_p % 4) return GSAMPLE_ERR_INVALID_ARG;
-  gsample_status st = check_common(logits, dtype, B, V, ld, out_idx, workspace);
-  if (st != GSAMPLE_OK || B == 0) return st;
-  const DeviceInfo* d = nullptr;
-  st = device_info(&d);
-  if (st != GSAMPLE_OK) return st;
-  // The proposals: the plain sampler over every row.
-  st = run_sample(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, workspace, 0,
-                  (cudaStream_t)stream);
-  if (st != GSAMPLE_OK || (!top_k && !top_p)) return st;
-  const bool vec = vec_path(logits, dtype, ld);
-  const int epu = gsample::units_elems((int)dtype, vec);
-  gsample::FilterParams fp;
-  fp.logits = static_cast<const char*>(logits);
-  fp.ld_bytes = ld * elt_bytes(dtype);
-  fp.B = B;
-  fp.V = (int32_t)V;
-  fp.units_per_row = (int32_t)((V + epu - 1) / epu);
-  fp.temperature = temperature;
-  fp.seed = seed;
-  fp.offset = offset;
-  fp.top_k = top_k;
-  fp.top_p = top_p;
-  fp.out_idx = out_idx;
-  fp.ws = static_cast<WsRow*>(workspace);
-  if (gsample::launch_filter(fp, (int)dtype, vec, (cudaStream_t)stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GSAMPLE_ERR_CUDA;
-  }
-  return GSAMPLE_OK;
+  return run_filtered(logits, dtype, B, V, ld, temperature, seed, offset, top_k, top_p, out_idx,
+                      workspace, 0, (cudaStream_t)stream);
 }
 
 gsample_status gsample_gumbel_argmax_host(const void* logits, gsample_dtype dtype, int64_t B,
@@ -697,6 +754,16 @@ gsample_status gsample_debug_categorical_ex(const void* logits, gsample_dtype dt
   if (cluster < 0) return GSAMPLE_ERR_INVALID_ARG;
   return run_categorical(logits, dtype, B, V, ld, temperature, seed, offset, out_idx, cluster,
                          (cudaStream_t)stream);
+}
+
+gsample_status gsample_debug_filtered_ex(const void* logits, gsample_dtype dtype, int64_t B,
+                                         int64_t V, int64_t ld, const float* temperature,
+                                         const uint64_t* seed, const uint64_t* offset,
+                                         const int32_t* top_k, const float* top_p,
+                                         int64_t* out_idx, void* workspace, int32_t cluster,
+                                         gsample_stream_t stream) {
+  return run_filtered(logits, dtype, B, V, ld, temperature, seed, offset, top_k, top_p, out_idx,
+                      workspace, cluster, (cudaStream_t)stream);
 }
 
 int32_t gsample_debug_planned_ctas(gsample_dtype dtype, int64_t B, int64_t V, int64_t ld,

@@ -82,22 +82,31 @@ struct RowClusterParams {
 };
 
 // Top-k / top-p on the Gumbel path, after the plain sampler has written its
-// proposals into out_idx: one CTA per row checks the proposal, then one CTA
-// per rejected row (flagged in ws[b].hint) resolves it exactly.
+// proposals into out_idx: one thread-block cluster of `cluster` CTAs per row
+// tests the proposal and, when it is rejected, replaces it by the Gumbel-max
+// over the filter set.
 struct FilterParams {
   const char* logits;
   int64_t ld_bytes;
   int64_t B;
   int32_t V;
   int32_t units_per_row;
+  int32_t cluster;
+  int32_t units_per_cta;
+  float mass_scale;      // 2^E: fixed-point unit of the top_p masses (a row's sum fits in 63 bits)
   const float* temperature;
   const uint64_t* seed;
   const uint64_t* offset;
   const int32_t* top_k;  // nullptr: no top-k
   const float* top_p;    // nullptr: no top-p
   int64_t* out_idx;
-  WsRow* ws;
 };
+// The filter kernel of (dtype, vec, resident) and its block size (occupancy
+// queries), the largest cluster the device co-schedules for it, and the
+// largest slice it holds in shared memory.
+void* filter_kernel_fn(int dtype, bool vec, bool resident, int* threads);
+int filter_max_cluster(int dtype, bool vec);
+size_t filter_smem_limit();
 cudaError_t launch_filter(const FilterParams& p, int dtype, bool vec, cudaStream_t stream);
 
 // Elements per unit for a dtype code (0 f32, 1 bf16, 2 f16) and load path.
