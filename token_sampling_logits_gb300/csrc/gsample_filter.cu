@@ -113,6 +113,7 @@ struct Partial {
   float mb;      // the same for the candidates before the proposal
   float M;       // largest logit
   unsigned cnt;  // candidates before the proposal
+  unsigned nl;   // candidates at or above the proposal (the floor set)
 };
 
 // Order-preserving keys in the bits the logit's dtype can set: a bf16 logit
@@ -258,10 +259,11 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
   __shared__ unsigned s_loff[kMaxCluster + 1];  // offsets of the CTAs' lists in rank 0's gather
   __shared__ unsigned s_tie[2];         // entries equal to K's last key before this slice, in it
   __shared__ int32_t s_idx;
+  __shared__ unsigned s_tcnt;           // entries on K's last key, gathered for one warp
+  __shared__ uint32_t s_tidx[32];
   __shared__ unsigned long long s_best[kFiltWarps];
   __shared__ unsigned long long s_key;  // this CTA's best (score, index) key, read by rank 0
 
-  pdl_wait_then_release();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int nrank = fp.cluster;
@@ -271,18 +273,20 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
   // early exits below are taken by the whole cluster or by none of it.
   const RowFilter f = row_filter(fp, b);
   if (!(f.T > 0.0f) || !(f.k_on || f.p_on)) return;  // greedy or unfiltered: the proposal stands
-  const int64_t w = fp.out_idx[b];
-  if (w < 0) return;  // no candidate at all
   const char* row = fp.logits + b * fp.ld_bytes;
-  const float xw = elt_at<DT>(row, w);
-  if (xw == INFINITY) return;  // the first +inf entry heads the order
+  const uint64_t sd = __ldg(fp.seed + b), of = __ldg(fp.offset + b);
+  if (threadIdx.x == 0) s_ln = 0u;
   const int32_t u_lo = rank * fp.units_per_cta;
   const int32_t u_hi = min(fp.units_per_row, u_lo + fp.units_per_cta);
   const uint32_t slice = (uint32_t)__cvta_generic_to_shared(smem);
 
-  // The slice, requested at once. Each thread later reads back only the units
-  // it requested (unit u_lo + threadIdx.x + j * kFiltThreads), so its own
-  // cp.async wait is all the ordering it needs.
+  // The slice, requested at once, before the wait for the proposal: the logits
+  // do not depend on the kernel that writes it, so their stream overlaps that
+  // kernel's tail. Each thread later reads back only the units it requested
+  // (unit u_lo + threadIdx.x + j * kFiltThreads), so its own cp.async wait is
+  // all the ordering it needs; no CTA leaves with a copy in flight. This
+  // kernel does not release its own dependents early: a successor resident
+  // while the filter's later waves still need the SMs would take their room.
   if constexpr (RESIDENT) {
     const uint64_t pol = evict_first_policy();
     for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kFiltThreads) {
@@ -293,8 +297,14 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
         sts128(dst, load_unit<DT, VEC>(row, u, fp.V, pol));
     }
     cp_async_commit();
-    cp_async_wait<0>();
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t w = fp.out_idx[b];
+  const float xw = w >= 0 ? elt_at<DT>(row, w) : -INFINITY;
+  if constexpr (RESIDENT) cp_async_wait<0>();
+  // no candidate at all, or the first +inf entry heads the order: the proposal stands
+  if (w < 0 || xw == INFINITY) return;
+  __syncthreads();
   auto unit_at = [&](int32_t u) -> uint4 {
     if constexpr (RESIDENT)
       return lds128(slice + (uint32_t)(u - u_lo) * 16u);
@@ -304,8 +314,15 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
 
   // 1. The test. Masses are relative to the proposal's (binary32, e^((x - xw)/T)
   // <= e^19.5 since no logit can outscore the proposal by more than the range
-  // of the Gumbel noise); a NaN logit adds nothing.
+  // of the Gumbel noise); a NaN logit adds nothing. A resident slice also lists
+  // its floor set (candidates at or above the proposal) as (key, index), in
+  // case the proposal is rejected.
   const float a = kLog2e / f.T;
+  // mass(x) = 2^(x*a - xw*a): the one rounding of xw*a scales every mass
+  // alike, so it cancels out of the test; a NaN or -inf logit gives 2^-127,
+  // flushed to zero.
+  const float nxa = -(xw * a);
+  auto mass_w = [&](float x) { return ex2_approx(fmaxf(fmaf(x, a, nxa), -127.0f)); };
   unsigned cnt = 0;
   float S = 0.0f, mb = 0.0f, tmax = -INFINITY;
   uint64_t marks = 0;  // bit j: the thread's j-th unit holds a logit >= xw (j >= 64: visited anyway)
@@ -318,7 +335,7 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
       for (int e = 0; e < EPU; ++e) {
         const float x = elt<DT, VEC>(r, e);
         um = fmaxf(um, x);
-        if (f.p_on) S += fmaxf(ex2_approx((x - xw) * a), 0.0f);
+        if (f.p_on) S += mass_w(x);
       }
       tmax = fmaxf(tmax, um);
       if (um >= xw) {
@@ -327,9 +344,15 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
         for (int e = 0; e < EPU; ++e) {
           const float x = elt<DT, VEC>(r, e);
           const int64_t i = (int64_t)u * EPU + e;
-          if (x > xw || (x == xw && i < w)) {
-            ++cnt;
-            if (f.p_on) mb += ex2_approx((x - xw) * a);
+          if (x >= xw) {
+            if constexpr (RESIDENT) {
+              const unsigned pos = atomicAdd(&s_ln, 1u);
+              if (pos < (unsigned)kLocalCap) s_list[pos] = make_uint2(ordered_bits(x), (uint32_t)i);
+            }
+            if (x > xw || i < w) {
+              ++cnt;
+              if (f.p_on) mb += mass_w(x);
+            }
           }
         }
       }
@@ -342,7 +365,7 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
     mb += __shfl_xor_sync(0xFFFFFFFFu, mb, o);
     tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, o));
   }
-  if (lane == 0) s_wp[warp] = Partial{S, mb, tmax, cnt};
+  if (lane == 0) s_wp[warp] = Partial{S, mb, tmax, cnt, 0u};
   __syncthreads();
   if (threadIdx.x == 0) {
     Partial t = s_wp[0];
@@ -352,12 +375,13 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
       t.M = fmaxf(t.M, s_wp[i].M);
       t.cnt += s_wp[i].cnt;
     }
+    t.nl = s_ln;
     s_part = t;
   }
   cluster.sync();
   if (warp == 0) {
     // the cluster's partials summed in rank order: every CTA rounds the same way
-    Partial o{0.0f, 0.0f, -INFINITY, 0u};
+    Partial o{0.0f, 0.0f, -INFINITY, 0u, 0u};
     if (lane < nrank) o = *cluster.map_shared_rank(&s_part, lane);
     Partial t = o;
     for (int q = 1; q < nrank; ++q) {
@@ -367,6 +391,19 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
       t.cnt += __shfl_sync(0xFFFFFFFFu, o.cnt, q);
     }
     if (lane == 0) s_tot = t;
+    // the CTAs' lists: offsets in rank 0's gather, total and largest
+    unsigned incl = o.nl, mx = o.nl;
+#pragma unroll
+    for (int q = 1; q < 32; q <<= 1) {
+      const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, q);
+      if (lane >= q) incl += v;
+      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, q));
+    }
+    if (lane <= nrank) s_loff[lane] = incl - o.nl;
+    if (lane == 31) {
+      s_lists[0] = incl;
+      s_lists[1] = mx;
+    }
   }
   __syncthreads();
   const Partial tot = s_tot;
@@ -399,46 +436,8 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
     m_rem = (unsigned long long)ceil((double)f.p * Sf);
     if (m_rem < 1ull) m_rem = 1ull;
   }
-  const uint64_t sd = __ldg(fp.seed + b), of = __ldg(fp.offset + b);
   const PhiloxRow ph =
       philox_row((uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32), (uint32_t)sd, (uint32_t)(sd >> 32));
-
-  // The floor set of a resident slice, listed as (key, index) for rank 0.
-  if (threadIdx.x == 0) s_ln = 0u;
-  __syncthreads();
-  if constexpr (RESIDENT) {
-    int j = 0;
-    for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kFiltThreads, ++j) {
-      if (j < 64 && !((marks >> j) & 1ull)) continue;
-      const uint4 r = unit_at(u);
-#pragma unroll
-      for (int e = 0; e < EPU; ++e) {
-        const float x = elt<DT, VEC>(r, e);
-        const uint32_t key = ordered_bits(x);
-        if (is_candidate(x) && key >= key_w) {
-          const unsigned pos = atomicAdd(&s_ln, 1u);
-          if (pos < (unsigned)kLocalCap) s_list[pos] = make_uint2(key, (uint32_t)(u * EPU + e));
-        }
-      }
-    }
-  }
-  cluster.sync();
-  if (warp == 0) {
-    const unsigned n = lane < nrank ? *cluster.map_shared_rank(&s_ln, lane) : 0u;
-    unsigned incl = n, mx = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += t;
-      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    }
-    if (lane <= nrank) s_loff[lane] = incl - n;
-    if (lane == 31) {
-      s_lists[0] = incl;
-      s_lists[1] = mx;
-    }
-  }
-  __syncthreads();
   const unsigned n_all = s_lists[0];
   if (RESIDENT && s_lists[1] <= (unsigned)kLocalCap && n_all <= 2u * (unsigned)fp.units_per_cta) {
     // 2a. Rank 0 gathers the cluster's lists into its slice buffer, the other
@@ -512,7 +511,29 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
     // K takes the first n_take entries on key_b in index order: the n_take-th
     // largest inverted index, eight bits a level.
     int32_t idx_b = INT32_MAX;
-    if (n_take < t_b) {
+    if (n_take < t_b && t_b <= 32u) {
+      // few entries on key_b: one warp ranks their indices
+      if (threadIdx.x == 0) {
+        s_tcnt = 0u;
+        s_idx = INT32_MAX;
+      }
+      __syncthreads();
+      for (unsigned i = threadIdx.x; i < n_all; i += kFiltThreads) {
+        if (lst[i].x == key_b) {
+          const unsigned pos = atomicAdd(&s_tcnt, 1u);
+          if (pos < 32u) s_tidx[pos] = lst[i].y;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t v = lane < (int)t_b ? s_tidx[lane] : 0xFFFFFFFFu;
+        unsigned r = 0;
+        for (unsigned q = 0; q < t_b; ++q) r += s_tidx[q] < v ? 1u : 0u;
+        if (lane < (int)t_b && r == n_take - 1u) s_idx = (int32_t)v;
+      }
+      __syncthreads();
+      idx_b = s_idx;
+    } else if (n_take < t_b) {
       unsigned kk = n_take;
       uint32_t ip = 0;
       bool found = true;
