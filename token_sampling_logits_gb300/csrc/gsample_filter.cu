@@ -345,7 +345,9 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
           const float x = elt<DT, VEC>(r, e);
           const int64_t i = (int64_t)u * EPU + e;
           if (x >= xw) {
-            if constexpr (RESIDENT) {
+            // once the list is full the row cannot take the list path, so
+            // a long floor set stops contending for the counter
+            if (RESIDENT && *reinterpret_cast<volatile unsigned*>(&s_ln) < (unsigned)kLocalCap) {
               const unsigned pos = atomicAdd(&s_ln, 1u);
               if (pos < (unsigned)kLocalCap) s_list[pos] = make_uint2(ordered_bits(x), (uint32_t)i);
             }
@@ -439,7 +441,9 @@ __global__ void __launch_bounds__(kFiltThreads, 4) filter_cluster_kernel(const F
   const PhiloxRow ph =
       philox_row((uint32_t)b, (uint32_t)of, (uint32_t)(of >> 32), (uint32_t)sd, (uint32_t)(sd >> 32));
   const unsigned n_all = s_lists[0];
-  if (RESIDENT && s_lists[1] <= (unsigned)kLocalCap && n_all <= 2u * (unsigned)fp.units_per_cta) {
+  // A CTA whose count reached kLocalCap may have skipped entries: that row
+  // takes the cluster-wide select.
+  if (RESIDENT && s_lists[1] < (unsigned)kLocalCap && n_all <= 2u * (unsigned)fp.units_per_cta) {
     // 2a. Rank 0 gathers the cluster's lists into its slice buffer, the other
     // CTAs leave, and rank 0 resolves the row alone.
     uint2* lst = reinterpret_cast<uint2*>(smem);
