@@ -611,7 +611,7 @@ def extra_table(dist: Dist, l2: int):
                "frac_of_8TBps": round(nbytes / us / 1e3 / 8000, 4),
                "single_launch_us": round(one, 3) if one is not None else None}
         if kind == "filtered":
-            row["filters"] = "top_k=50, top_p=0.9 on every row (three launches per step)"
+            row["filters"] = "top_k=50, top_p=0.9 on every row (two launches per step: proposal, filter)"
         if kind == "sweep":
             # The issue's comparison: the categorical (softmax + inverse-CDF)
             # path against Gumbel-max on the same V x B grid.

@@ -174,7 +174,8 @@ int pick_cluster(void* (*kernel)(int, bool, bool, int*), int dtype, bool vec, in
 // The filter's cluster size for B rows of nu units: the smallest power of two
 // (at most max_cluster) whose slices fit in GSAMPLE_FILT_SLICE_BYTES of shared
 // memory, so that several CTAs share an SM; then doubled while the whole batch
-// still runs in one wave and every CTA keeps a unit per thread.
+// still runs in two waves of clusters and every CTA keeps a unit per thread
+// (measured at V = 152K bf16: 16 CTAs per row at B = 64, 8 from B = 128).
 int pick_filter_cluster(int dtype, bool vec, int64_t B, int64_t nu, int max_cluster) {
   const size_t limit = gsample::filter_smem_limit();
   int c = 1;
@@ -188,7 +189,8 @@ int pick_filter_cluster(int dtype, bool vec, int64_t B, int64_t nu, int max_clus
     const size_t smem = (size_t)upc * 16;
     const bool resident = smem <= limit;
     void* fn = gsample::filter_kernel_fn(dtype, vec, resident, &threads);
-    if (upc < threads || B > active_clusters(fn, threads, c2, resident ? smem : 0)) break;
+    if (upc < threads || B > 2 * (int64_t)active_clusters(fn, threads, c2, resident ? smem : 0))
+      break;
     c = c2;
   }
   return c;
