@@ -126,6 +126,19 @@ __device__ __forceinline__ unsigned long long block_best(float s, int32_t i,
   return k;
 }
 
+// Packed maxima of two pairs of 16-bit logits (bf16 when DT is 1, else f16).
+template <int DT>
+__device__ __forceinline__ uint32_t hlg_hmax2(uint32_t a, uint32_t b) {
+  if constexpr (DT == 1) {
+    __nv_bfloat162 m = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                               *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&m);
+  } else {
+    __half2 m = __hmax2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&m);
+  }
+}
+
 template <int DT, bool VEC, bool RESIDENT>
 __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   using C = HCfg<DT, VEC>;
@@ -197,22 +210,44 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   // The thread's largest logit (lowest index on ties): the greedy answer, and
   // the first exact candidate of a sampled row. For the pivot, the largest
   // finite logit; +inf is flagged.
+  // Unit maxima first (NaN is ignored unless a whole unit is NaN, and a NaN
+  // maximum never wins); a unit holding +inf takes its finite maximum element
+  // by element; then the first element of the best unit that equals its max.
   float cand_x = -INFINITY;
-  int32_t cand_i = INT32_MAX;
+  int32_t cand_u = -1;
   float fmax_x = -INFINITY;
   bool pinf = false;
   for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
     const uint4 r = unit_at(u);
-#pragma unroll
-    for (int e = 0; e < C::kEPU; ++e) {
-      const float x = elt<DT, VEC>(r, e);
-      if (x > cand_x) {
-        cand_x = x;
-        cand_i = u * C::kEPU + e;
-      }
-      if (x == INFINITY) pinf = true;
-      else fmax_x = fmaxf(fmax_x, x);
+    float m;
+    if constexpr (C::kF32Bits) {
+      m = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+    } else {
+      const uint32_t h = hlg_hmax2<DT>(hlg_hmax2<DT>(r.x, r.y), hlg_hmax2<DT>(r.z, r.w));
+      m = fmaxf(half_to_f32<DT>(h & 0xFFFFu), half_to_f32<DT>(h >> 16));
     }
+    if (m > cand_x) {
+      cand_x = m;
+      cand_u = u;
+    }
+    if (m == INFINITY) {
+      pinf = true;
+#pragma unroll
+      for (int e = 0; e < C::kEPU; ++e) {
+        const float x = elt<DT, VEC>(r, e);
+        if (x != INFINITY) fmax_x = fmaxf(fmax_x, x);
+      }
+    } else {
+      fmax_x = fmaxf(fmax_x, m);
+    }
+  }
+  int32_t cand_i = INT32_MAX;
+  if (cand_u >= 0) {
+    const uint4 r = unit_at(cand_u);
+#pragma unroll
+    for (int e = C::kEPU - 1; e >= 0; --e)
+      if (elt<DT, VEC>(r, e) == cand_x) cand_i = cand_u * C::kEPU + e;
   }
 
   float bs = -INFINITY;
