@@ -127,6 +127,38 @@ def test_signed_zeros_tie():
         _check(bs, np.full(B, 2, np.int32), None, t, "zeros cluster 2", cluster=2)
 
 
+def test_filtered_ld_and_misaligned_rows():
+    """Rows in a wider buffer (ld > V) and shifted by 1-3 elements: the filter
+    then takes the element-by-element load path for every dtype."""
+    B, V, ld = 5, 3001, 3008
+    rng = np.random.default_rng(12)
+    base = (rng.standard_normal((B, ld + 8)) * 2).astype(np.float32)
+    K = np.array([3, 0, 40, 1, 7], np.int32)
+    P = np.array([0.5, 0.9, 1.0, 0.2, 0.99], np.float32)
+    t = Tally()
+    for dtype in (W.F32, W.BF16, W.F16):
+        enc = W.encode(base, dtype)
+        dev = to_device(enc, dtype)
+        for shift in (0, 1, 3):
+            view = dev[:, shift:shift + V]
+            host = np.ascontiguousarray(enc[:, shift:shift + V])
+            T = np.array([0.5, 1.0, 0.0, 2.0, 1.5], np.float32)
+            b = W.Batch("ld", host, dtype, T, W.splitmix64(9, B), np.full(B, 7, np.uint64))
+            for step in range(3):
+                _check(b.at_step(step), K, P, t, "ld shift=%d dt=%d" % (shift, dtype), x=view)
+    register("6 filtered (edge cases)", t, assert_bound=False)
+
+
+def test_filtered_large_batch():
+    """4100 rows (32,800 CTAs of filter clusters) with mixed filters."""
+    b, rng = _small(4100, 1000, W.BF16, 21)
+    K = rng.choice([0, 1, 5, 50], b.B).astype(np.int32)
+    P = rng.choice([1.0, 0.5, 0.9], b.B).astype(np.float32)
+    t = Tally()
+    _check(b, K, P, t, "B=4100")
+    register("6 filtered (edge cases)", t, assert_bound=False)
+
+
 def test_rejections_and_acceptances_both_exercised():
     """Flat rows with a tight top-k reject nearly every proposal (the exact
     path); one dominant logit makes every proposal stand (the fast path)."""
