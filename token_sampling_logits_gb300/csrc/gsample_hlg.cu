@@ -39,6 +39,9 @@ namespace {
 using namespace slice;
 
 constexpr int kHlgThreads = 512;
+#ifndef GSAMPLE_HLG_CHUNKS
+#define GSAMPLE_HLG_CHUNKS 4
+#endif
 constexpr int kHlgWarps = kHlgThreads / 32;
 
 // Online softmax moments of finite logits: M = max x, S = sum e^(x-M),
@@ -188,19 +191,9 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   const bool entropy = hp.pivot_mode == 1;
   if (threadIdx.x == 0) s_pinf = 0;
 
-  // Sweep 1: stream the slice once. On the resident path every unit of the
-  // thread's share is requested at once (cp.async into the slice), so the whole
-  // slice is in flight together; the thread then reads back its own units.
-  if constexpr (RESIDENT) {
-    for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
-      const uint32_t dst = slice + (uint32_t)(u - u_lo) * 16u;
-      if (VEC && (u + 1) * C::kEPU <= p.V)
-        cp_async16(dst, row + (size_t)u * 16, pol);
-      else
-        sts128(dst, load_unit<DT, VEC>(row, u, p.V, pol));
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  }
+  // Sweep 1: stream the slice once. On the resident path the thread's whole
+  // share is requested with cp.async into the slice, so the whole slice is in
+  // flight together; the thread reads back its own units as they land.
   auto unit_at = [&](int32_t u) -> uint4 {
     if constexpr (RESIDENT)
       return lds128(slice + (uint32_t)(u - u_lo) * 16u);
@@ -217,8 +210,7 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
   int32_t cand_u = -1;
   float fmax_x = -INFINITY;
   bool pinf = false;
-  for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) {
-    const uint4 r = unit_at(u);
+  auto sweep1_unit = [&](int32_t u, const uint4& r) {
     float m;
     if constexpr (C::kF32Bits) {
       m = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
@@ -241,6 +233,15 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
     } else {
       fmax_x = fmaxf(fmax_x, m);
     }
+  };
+  // On the resident path the thread's units are requested in GSAMPLE_HLG_CHUNKS
+  // groups (the whole slice is in flight together) and each group is reduced
+  // as it lands.
+  if constexpr (RESIDENT) {
+    load_slice_then<DT, VEC, kHlgThreads, GSAMPLE_HLG_CHUNKS>(row, u_lo, u_hi, p.V, slice, pol,
+                                                             sweep1_unit);
+  } else {
+    for (int32_t u = u_lo + threadIdx.x; u < u_hi; u += kHlgThreads) sweep1_unit(u, unit_at(u));
   }
   int32_t cand_i = INT32_MAX;
   if (cand_u >= 0) {

@@ -29,6 +29,9 @@ namespace {
 using namespace slice;
 
 constexpr int kRcThreads = 512;
+#ifndef GSAMPLE_RC_CHUNKS
+#define GSAMPLE_RC_CHUNKS 4
+#endif
 constexpr int kRcWarps = kRcThreads / 32;
 
 // Packed maxima of two pairs of 16-bit logits (bf16 when DT is 1, else f16).
@@ -81,18 +84,6 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
   const uint64_t sd = p.seed ? __ldg(p.seed + b) : 0ull;
   const uint64_t of = p.offset ? __ldg(p.offset + b) : 0ull;
 
-  // Every unit of the thread's share is requested at once; the thread then
-  // reads back its own units only, so its own wait is enough.
-  if constexpr (RESIDENT) {
-    for (int32_t u = u_lo + tid; u < u_hi; u += kRcThreads) {
-      const uint32_t dst = slice + (uint32_t)(u - u_lo) * 16u;
-      if (VEC && (u + 1) * C::kEPU <= p.V)
-        cp_async16(dst, row + (size_t)u * 16, pol);
-      else
-        sts128(dst, load_unit<DT, VEC>(row, u, p.V, pol));
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  }
   auto unit_at = [&](int32_t u) -> uint4 {
     if constexpr (RESIDENT)
       return lds128(slice + (uint32_t)(u - u_lo) * 16u);
@@ -104,11 +95,11 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
   // the first exact candidate of a sampled row. Unit maxima first (packed
   // half2 maxima for 16-bit logits; NaN is ignored unless a whole unit is NaN,
   // and a NaN maximum never wins), then the first element of the best unit
-  // that equals it.
+  // that equals it. On the resident path the thread's units are requested in
+  // GSAMPLE_RC_CHUNKS groups and each is reduced as it lands.
   float cand_x = -INFINITY;
   int32_t cand_u = -1;
-  for (int32_t u = u_lo + tid; u < u_hi; u += kRcThreads) {
-    const uint4 r = unit_at(u);
+  auto unit_max_of = [&](int32_t u, const uint4& r) {
     float m;
     if constexpr (C::kF32Bits) {
       m = fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
@@ -121,6 +112,12 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
       cand_x = m;
       cand_u = u;
     }
+  };
+  if constexpr (RESIDENT) {
+    load_slice_then<DT, VEC, kRcThreads, GSAMPLE_RC_CHUNKS>(row, u_lo, u_hi, p.V, slice, pol,
+                                                           unit_max_of);
+  } else {
+    for (int32_t u = u_lo + tid; u < u_hi; u += kRcThreads) unit_max_of(u, unit_at(u));
   }
   int32_t cand_i = INT32_MAX;
   if (cand_u >= 0) {

@@ -61,5 +61,57 @@ __device__ __forceinline__ uint4 load_unit(const char* row, int32_t u, int32_t V
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// cp.async.wait_group with a count known only after unrolling.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
+}
+
+// The thread's units of the slice [u_lo, u_hi) (u_lo + tid, then every
+// THREADS-th unit) are requested into shared memory in CHUNKS commit groups,
+// in unit order; then f(u, unit) runs on each unit, in the same order, as soon
+// as its chunk has landed, so the work on the first chunks overlaps the
+// arrival of the later ones. Units past V read as -inf. Each thread reads back
+// only its own units, so its own wait suffices.
+template <int DT, bool VEC, int THREADS, int CHUNKS, typename F>
+__device__ __forceinline__ void load_slice_then(const char* row, int32_t u_lo, int32_t u_hi,
+                                                int32_t V, uint32_t slice, uint64_t pol, F&& f) {
+  static_assert(CHUNKS >= 1 && CHUNKS <= 8, "one to eight commit groups");
+  constexpr int EPU = HCfg<DT, VEC>::kEPU;
+  const int tid = threadIdx.x;
+  const int32_t n = u_hi - u_lo > tid ? (u_hi - u_lo - tid + THREADS - 1) / THREADS : 0;
+  const int32_t per = (n + CHUNKS - 1) / CHUNKS;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const int32_t i1 = min(n, (c + 1) * per);
+    for (int32_t i = c * per; i < i1; ++i) {
+      const int32_t u = u_lo + tid + i * THREADS;
+      const uint32_t dst = slice + (uint32_t)(u - u_lo) * 16u;
+      if (VEC && (u + 1) * EPU <= V)
+        cp_async16(dst, row + (size_t)u * 16, pol);
+      else
+        sts128(dst, load_unit<DT, VEC>(row, u, V, pol));
+    }
+    cp_async_commit();
+  }
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    cp_async_wait_upto(CHUNKS - 1 - c);
+    const int32_t i1 = min(n, (c + 1) * per);
+    for (int32_t i = c * per; i < i1; ++i) {
+      const int32_t u = u_lo + tid + i * THREADS;
+      f(u, lds128(slice + (uint32_t)(u - u_lo) * 16u));
+    }
+  }
+}
+
 }  // namespace slice
 }  // namespace gsample
