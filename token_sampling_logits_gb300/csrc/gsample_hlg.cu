@@ -115,6 +115,14 @@ __device__ __forceinline__ float hlg_score(const Curve& c, const RowState& rs, f
   return __fdiv_rn(y, T) + gumbel_of_word(word);
 }
 
+// The same score with the Gumbel value g already computed from the word.
+__device__ __forceinline__ float hlg_score_g(const Curve& c, const RowState& rs, float x, float g,
+                                             float T) {
+  if (x == INFINITY) return INFINITY;
+  const float y = tone(c, x + rs.shift);
+  return __fdiv_rn(y, T) + g;
+}
+
 // Block-wide (score, index) argmax; every thread gets the result. `red` holds
 // kHlgWarps packed keys.
 __device__ __forceinline__ unsigned long long block_best(float s, int32_t i,
@@ -257,6 +265,16 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
     bs = cand_x;
     bi = cand_x > -INFINITY ? cand_i : INT32_MAX;
   } else {
+    const uint32_t k0 = (uint32_t)sd, k1 = (uint32_t)(sd >> 32);
+    const uint32_t o0 = (uint32_t)of, o1 = (uint32_t)(of >> 32);
+    const PhiloxRow ph = philox_row((uint32_t)b, o0, o1, k0, k1);
+    // The first candidate's Gumbel value does not depend on the pivot, so its
+    // Philox block and logarithms run before the pivot exchange and overlap it.
+    float cand_g = 0.0f;
+    if (cand_i != INT32_MAX && cand_x > -INFINITY) {
+      const uint4 blk = philox_row_1((uint32_t)cand_i >> 2, ph);
+      cand_g = gumbel_of_word(word_of(blk, cand_i & 3));
+    }
     // Pivot statistics of the slice. Entropy: a second pass over the slice
     // (shared memory) sums e^(x - M) and e^(x - M) x against the thread's max.
     Moments mo{fmax_x, 0.0f, 0.0f};
@@ -328,17 +346,11 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
 
     const Curve cv{hp.m, hp.w, hp.beta_t, hp.beta_h, 1.0f / hp.beta_t, 1.0f / hp.beta_h};
     const float rT = 1.0f / T;
-    const uint32_t k0 = (uint32_t)sd, k1 = (uint32_t)(sd >> 32);
-    const uint32_t o0 = (uint32_t)of, o1 = (uint32_t)(of >> 32);
-    const uint32_t row_id = (uint32_t)b;
-    const PhiloxRow ph = philox_row(row_id, o0, o1, k0, k1);
 
     // First candidate: this thread's largest logit, scored exactly; the CTA's
     // best of them is the bound L that sweep 2 prunes against.
-    if (cand_i != INT32_MAX && cand_x > -INFINITY && (!rs.pinf || cand_x == INFINITY)) {
-      const uint4 blk = philox_row_1((uint32_t)cand_i >> 2, ph);
-      take_better(hlg_score(cv, rs, cand_x, word_of(blk, cand_i & 3), T), cand_i, bs, bi);
-    }
+    if (cand_i != INT32_MAX && cand_x > -INFINITY && (!rs.pinf || cand_x == INFINITY))
+      take_better(hlg_score_g(cv, rs, cand_x, cand_g, T), cand_i, bs, bi);
     // The bound: the best first candidate of the whole row, over the cluster.
     {
       const unsigned long long kc = block_best(bs, bi, s_red);
