@@ -447,9 +447,10 @@ __device__ __forceinline__ void compact_batch(uint32_t stage, const unsigned sho
 #endif
 
 // A sampled tile. Each lane first takes the largest logit of each of its
-// groups; when none in the warp reaches the logit threshold the tile is
-// skipped. The share of groups that do is estimated from 128 of them (each
-// lane's first four). A large share (above GSAMPLE_DENSE_NUM/DEN): every group
+// groups. The share of groups that reach the logit threshold is estimated from
+// 128 of them (each lane's first four); when none of those does, the whole
+// tile is tested and skipped if no group in the warp reaches it. A large
+// share (above GSAMPLE_DENSE_NUM/DEN): every group
 // gets its Philox block, four per lane side by side, as straight-line code.
 // Otherwise the survivors' tile-local indices are compacted into a list and
 // only they get Philox, 128 per warp batch (a short last batch runs one or two
@@ -477,17 +478,21 @@ __device__ __forceinline__ void sampled_tile(uint32_t stage, uint32_t g0, const 
       xm[2 * k + 1] = fmaxf(half_to_f32<DT>(m1 & 0xFFFFu), half_to_f32<DT>(m1 >> 16));
     }
   }
-  float tm = xm[0];
-#pragma unroll
-  for (int i = 1; i < NG; ++i) tm = fmaxf(tm, xm[i]);
-  if (!__any_sync(0xFFFFFFFFu, tm >= pr.thr_x)) return;  // nothing here can win
-  const ReachTest rt = make_reach(pr, rc.rT);
-
-  // The share of surviving groups, estimated from each lane's first four.
+  // The share of surviving groups, estimated from each lane's first four. Only
+  // when none of those survives is the whole tile tested for a skip (at
+  // moderate and high temperatures the sample almost always holds survivors,
+  // and the tile's maximum is not needed).
   int c4 = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) c4 += xm[i] >= pr.thr_x ? 1 : 0;
   const int sample = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)c4);
+  if (sample == 0) {
+    float tm = xm[0];
+#pragma unroll
+    for (int i = 1; i < NG; ++i) tm = fmaxf(tm, xm[i]);
+    if (!__any_sync(0xFFFFFFFFu, tm >= pr.thr_x)) return;  // nothing here can win
+  }
+  const ReachTest rt = make_reach(pr, rc.rT);
   if (sample * GSAMPLE_DENSE_DEN > 128 * GSAMPLE_DENSE_NUM) {
     // Every group's word threshold first: it needs only the logits, so its
     // exponential runs ahead of, not after, the Philox chains.
