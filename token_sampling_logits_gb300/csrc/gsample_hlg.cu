@@ -123,6 +123,40 @@ __device__ __forceinline__ float hlg_score_g(const Curve& c, const RowState& rs,
   return __fdiv_rn(y, T) + g;
 }
 
+struct HlgBest {
+  float s;
+  int32_t i;
+};
+
+// The exact pass over a warp's listed groups, one group per lane: each
+// element's own word bound, then tone(z)/T + g. Out of line: it runs once per
+// 32 listed groups, and keeping its logarithms out of sweep 2 keeps that
+// loop's code small.
+__device__ __noinline__ HlgBest hlg_flush_cold(const uint32_t* rg, const float4* rx, const uint4* rw,
+                                               int rcnt, float x_thr, bool word_test, float wa,
+                                               float wc, Curve cv, RowState rs, float T, float bs,
+                                               int32_t bi) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane < rcnt) {
+    const uint32_t gg = rg[lane];
+    const float4 xx = rx[lane];
+    const uint4 ww = rw[lane];
+    const float xs[4] = {xx.x, xx.y, xx.z, xx.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float x = xs[t];
+      if (!(x >= x_thr) || x == -INFINITY) continue;
+      if (word_test &&
+          !may_reach(tone_upper(cv, x + rs.shift), word_of(ww, t), ReachTest{wa, wc}))
+        continue;
+      take_better(hlg_score(cv, rs, x, word_of(ww, t), T), (int32_t)(4 * gg + t), bs, bi);
+    }
+  }
+  __syncwarp();
+  return HlgBest{bs, bi};
+}
+
 // Block-wide (score, index) argmax; every thread gets the result. `red` holds
 // kHlgWarps packed keys.
 __device__ __forceinline__ unsigned long long block_best(float s, int32_t i,
@@ -393,23 +427,10 @@ __global__ void __launch_bounds__(kHlgThreads) hlg_kernel(const HlgParams p) {
     // word bound, then tone(z)/T + g.
     int rcnt = 0;
     auto flush = [&]() {
-      __syncwarp();
-      if (lane < rcnt) {
-        const uint32_t gg = s_rg[warp][lane];
-        const float4 xx = s_rx[warp][lane];
-        const uint4 ww = s_rw[warp][lane];
-        const float xs[4] = {xx.x, xx.y, xx.z, xx.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float x = xs[t];
-          if (!(x >= x_thr) || x == -INFINITY) continue;
-          if (word_test &&
-              !may_reach(tone_upper(cv, x + rs.shift), word_of(ww, t), ReachTest{wa, wc}))
-            continue;
-          take_better(hlg_score(cv, rs, x, word_of(ww, t), T), (int32_t)(4 * gg + t), bs, bi);
-        }
-      }
-      __syncwarp();
+      const HlgBest r = hlg_flush_cold(&s_rg[warp][0], &s_rx[warp][0], &s_rw[warp][0], rcnt, x_thr,
+                                       word_test, wa, wc, cv, rs, T, bs, bi);
+      bs = r.s;
+      bi = r.i;
     };
     for (int32_t it = 0; it < n_iter; it += kUPB) {
       uint4 r[kUPB];

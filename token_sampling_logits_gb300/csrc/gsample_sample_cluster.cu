@@ -47,6 +47,20 @@ __device__ __forceinline__ uint32_t rc_hmax2(uint32_t a, uint32_t b) {
   }
 }
 
+struct RcBest {
+  float s;
+  int32_t i;
+};
+
+// The rare exact scores of one group, out of line so that the sweep's loop
+// code stays small.
+__device__ __noinline__ RcBest rc_score_cold(uint32_t g, float x0, float x1, float x2, float x3,
+                                             uint4 w, Prune pr, ReachTest rt, float T, float bs,
+                                             int32_t bi) {
+  score_group(g, x0, x1, x2, x3, w, pr, rt, T, &bs, &bi);
+  return RcBest{bs, bi};
+}
+
 // Block-wide (score, index) argmax as a packed key; every thread gets it.
 __device__ __forceinline__ unsigned long long rc_block_best(float s, int32_t i,
                                                             unsigned long long* red) {
@@ -179,9 +193,21 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
         if (ok[jj] && max_word(w[jj]) >= wt[jj]) {
           const uint4 rj = r[jj / C::kGPU];
           const int h = jj % C::kGPU;
-          score_group(g[jj], elt<DT, VEC>(rj, 4 * h), elt<DT, VEC>(rj, 4 * h + 1),
-                      elt<DT, VEC>(rj, 4 * h + 2), elt<DT, VEC>(rj, 4 * h + 3), w[jj], pr, rt, T,
-                      &bs, &bi);
+          if constexpr (DT != 0) {
+            // 16-bit rows: the exact scores out of line (measured faster at
+            // B = 32-64); binary32 rows keep them inline (faster on the
+            // small f32 sweeps).
+            const RcBest sb = rc_score_cold(g[jj], elt<DT, VEC>(rj, 4 * h),
+                                            elt<DT, VEC>(rj, 4 * h + 1),
+                                            elt<DT, VEC>(rj, 4 * h + 2),
+                                            elt<DT, VEC>(rj, 4 * h + 3), w[jj], pr, rt, T, bs, bi);
+            bs = sb.s;
+            bi = sb.i;
+          } else {
+            score_group(g[jj], elt<DT, VEC>(rj, 4 * h), elt<DT, VEC>(rj, 4 * h + 1),
+                        elt<DT, VEC>(rj, 4 * h + 2), elt<DT, VEC>(rj, 4 * h + 3), w[jj], pr, rt, T,
+                        &bs, &bi);
+          }
         }
       }
     }
