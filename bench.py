@@ -753,7 +753,10 @@ def run_ours(args, dist: Dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        # the arithmetic the path computes in: binary32 scores (the bf16
+        # logits widened exactly) and 32-bit integer Philox words
+        "dtype": "f32",
+        "input_dtype": "bf16",
         "data": "synthetic",
         "config": headline_config(batch, dist.world),
         "setup": {"parallelism": "replicas x%d" % dist.world,
