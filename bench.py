@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--count-blocks", action="store_true",
                     help="build the block-counting variant of the library and print the Philox "
                          "blocks the sampler computes per launch of the headline batch")
+    ap.add_argument("--alu-probe", action="store_true",
+                    help="time gsample_debug_philox_alu_mix: Philox alone, ALU work alone and "
+                         "both, and print how much of the ALU work adds to the Philox time")
     ap.add_argument("--categorical", action="store_true",
                     help="with --workload: time the categorical (softmax + inverse-CDF) kernel")
     args = ap.parse_args()
@@ -828,6 +831,47 @@ def run_reference(args, dist: Dist):
     print(json.dumps(line), flush=True)
 
 
+def run_alu_probe(args):
+    """How much ALU work issued beside the Philox multiplies adds to their time
+    (gsample_debug_philox_alu_mix, 16 warps per SM as in the sampler): ns per
+    warp-block per SM sub-partition for Philox alone, the ALU updates alone and
+    both, and the share of the ALU time that the mixed run adds."""
+    import torch
+
+    import token_sampling_logits_gb300 as gs
+
+    L = gs.lib()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    w, iters = 16, 2000
+    sink = torch.empty(sms * w * 32, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+
+    def ns_per_warp_block(steps, philox):
+        times = []
+        for rep in range(4):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            rc = L.gsample_debug_philox_alu_mix(w, iters, steps, philox, sink.data_ptr(), st)
+            e1.record()
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError("gsample_debug_philox_alu_mix: " + gs.status_string(rc))
+            times.append(e0.elapsed_time(e1) * 1e6)
+        # each SM sub-partition runs w / 4 warps of iters * 4 blocks
+        return min(times[1:]) / (w / 4 * iters * 4)
+
+    res = {"warps_per_sm": w, "iters": iters, "unit": "ns per warp-block per SM sub-partition",
+           "philox_only": round(ns_per_warp_block(0, 1), 4)}
+    for steps in (2, 4):
+        alu = ns_per_warp_block(steps, 0)
+        mix = ns_per_warp_block(steps, 1)
+        res["alu_steps_%d" % steps] = {"alu_only": round(alu, 4), "mixed": round(mix, 4),
+                                       "added_share_of_alu": round((mix - res["philox_only"]) / alu,
+                                                                   3)}
+    print(json.dumps(res), flush=True)
+
+
 def run_count_blocks(args):
     """Philox blocks the sampler computes per launch of the headline batch, from
     a build of the library with a device counter (-DGSAMPLE_COUNT_BLOCKS, built
@@ -873,6 +917,9 @@ def main():
     args = parse_args()
     if args.count_blocks:
         run_count_blocks(args)
+        return
+    if args.alu_probe:
+        run_alu_probe(args)
         return
     dist = Dist(args.gpus)
     try:

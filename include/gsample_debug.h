@@ -90,6 +90,21 @@ gsample_status gsample_debug_filtered_ex(const void* logits, gsample_dtype dtype
 gsample_status gsample_debug_philox_rate(int32_t warps_per_sm, uint32_t iters, uint32_t* sink,
                                          gsample_stream_t stream);
 
+/* How ALU work adds to the Philox multiplies (a measurement probe, no page
+ * counterpart): one CTA per SM of warps_per_sm warps (1..32); each thread runs
+ * `iters` iterations of four blocks of the kernels' Philox block code (when
+ * with_philox is 1) and/or 4 * alu_steps independent ALU updates per block
+ * (alu_steps 0, 2 or 4; shifts and bitwise operations in four chains that do
+ * not depend on the Philox words), folding everything into sink[thread].
+ * sink: device uint32[SMs * warps_per_sm * 32]. Time the Philox-only,
+ * ALU-only and mixed shapes on `stream`: the mixed time minus the Philox-only
+ * time, over the ALU-only time, is the share of the ALU work that does not
+ * hide behind the multiplies. GSAMPLE_ERR_INVALID_ARG for other values or
+ * for alu_steps 0 without Philox. */
+gsample_status gsample_debug_philox_alu_mix(int32_t warps_per_sm, uint32_t iters,
+                                            int32_t alu_steps, int32_t with_philox,
+                                            uint32_t* sink, gsample_stream_t stream);
+
 /* Philox blocks the row sampler computed since the last reset (dense tiles,
  * compacted batches, first candidates and exact passes, summed over
  * launches), in a library built with -DGSAMPLE_COUNT_BLOCKS; reset != 0 sets

@@ -225,6 +225,22 @@ def test_philox_rate_and_block_counter_validation():
         assert L.gsample_debug_philox_rate(8, 10, FAKE, None) == gs.ERR_CUDA
 
 
+def test_philox_alu_mix_validation():
+    L = gs.lib()
+    f = L.gsample_debug_philox_alu_mix
+    assert f(0, 10, 2, 1, FAKE, None) == gs.ERR_INVALID_ARG
+    assert f(33, 10, 2, 1, FAKE, None) == gs.ERR_INVALID_ARG
+    assert f(16, 0, 2, 1, FAKE, None) == gs.ERR_INVALID_ARG
+    assert f(16, 10, 3, 1, FAKE, None) == gs.ERR_INVALID_ARG
+    assert f(16, 10, 2, 2, FAKE, None) == gs.ERR_INVALID_ARG
+    assert f(16, 10, 0, 0, FAKE, None) == gs.ERR_INVALID_ARG  # nothing to run
+    assert f(16, 10, 2, 1, None, None) == gs.ERR_INVALID_ARG
+    assert f(16, 10, 2, 1, FAKE + 2, None) == gs.ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert f(16, 10, 2, 1, FAKE, None) == gs.ERR_CUDA
+
+
 def test_hlg_score_debug_validation():
     L = gs.lib()
     hp = gs.HlgParams().to_c()

@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
                                                _vp, _vp, _i32, _vp]),
             "gsample_debug_planned_ctas": (_i32, [_int, _i64, _i64, _i64, _vp, _i32]),
             "gsample_debug_philox_rate": (_int, [_i32, _u32, _vp, _vp]),
+            "gsample_debug_philox_alu_mix": (_int, [_i32, _u32, _i32, _i32, _vp, _vp]),
             "gsample_debug_blocks_computed": (_int, [_vp, _i32]),
             "gsample_debug_hlg_score": (_int, [_vp, _vp, _i64, _vp, ctypes.c_float, ctypes.c_float,
                                                _vp, _vp]),
