@@ -172,14 +172,20 @@ __global__ void __launch_bounds__(kRcThreads, 1) sample_cluster_kernel(const Row
         const int32_t u = u_lo + tid + (it + j) * kRcThreads;
         const bool valid = u < u_hi;
         r[j] = valid ? unit_at(u) : make_uint4(0, 0, 0, 0);
+        if constexpr (C::kF32Bits) {
+          xm[j] = fmaxf(fmaxf(__uint_as_float(r[j].x), __uint_as_float(r[j].y)),
+                        fmaxf(__uint_as_float(r[j].z), __uint_as_float(r[j].w)));
+        } else {
+          // Packed maxima of each group's two element pairs, then the larger
+          // half (NaN is ignored unless all four are NaN, as with fmaxf).
+          const uint32_t m0 = rc_hmax2<DT>(r[j].x, r[j].y), m1 = rc_hmax2<DT>(r[j].z, r[j].w);
+          xm[2 * j] = fmaxf(half_to_f32<DT>(m0 & 0xFFFFu), half_to_f32<DT>(m0 >> 16));
+          xm[2 * j + 1] = fmaxf(half_to_f32<DT>(m1 & 0xFFFFu), half_to_f32<DT>(m1 >> 16));
+        }
 #pragma unroll
         for (int h = 0; h < C::kGPU; ++h) {
-          float gm = elt<DT, VEC>(r[j], 4 * h);
-#pragma unroll
-          for (int e = 1; e < 4; ++e) gm = fmaxf(gm, elt<DT, VEC>(r[j], 4 * h + e));
           const int jj = j * C::kGPU + h;
-          xm[jj] = gm;
-          ok[jj] = valid && gm >= pr.thr_x;
+          ok[jj] = valid && xm[jj] >= pr.thr_x;
           g[jj] = (uint32_t)(u * C::kGPU + h);
         }
       }
